@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Decode throughput of the 35B-tier 40-layer int4 MoE stack at batch 1.
+
+One step = 256 consecutive decode tokens of an AR(1) token stream through the
+40 layers (H=2048, I=512, E=256, softmax-top-4, shared expert with an
+unmerged rank-16 LoRA, 33 prerouter heads owned by layers 6..38 whose
+predictions route layers 7..39 one token later).  Each token is one launch of
+the persistent whole-token kernel.  Weights are synthetic (seeded), resident in
+HBM (18.1 GB expert bank); every token streams ~484 MB of weights, far more
+than the 129 MB L2, so no flush is needed between iterations.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Under torchrun every rank runs an independent replica ("replicas only": the
+path has no cross-GPU exchange); value = all ranks' tokens / max rank time.
+The reference arm (--impl reference) times the CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s + expert-weight HBM GB/s (35B-tier MoE stack, batch 1)"
+WORKLOAD = ("35B-tier 40-layer MoE stack decode, batch 1: H=2048, I=512, E=256, softmax-top-k K=4, "
+            "shared expert + unmerged LoRA r=16 alpha=32, 33 prerouter heads (owners 6..38, hidden 512), "
+            "AR(1) rho=0.8 token stream")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--tokens-per-step", type=int, default=256)
+    p.add_argument("--no-cpu", action="store_true", help="skip the timed CPU-oracle baseline")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--kernel-impl", type=int, default=0, help="0 persistent kernel, 1 per-phase chain")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+
+def bytes_per_token(shape, native_layers: int):
+    """Weight bytes one steady-state token must read (each selected expert
+    counted once), split by kind."""
+    from int4_gathered_expert_gb300 import synth
+    s = shape.layer
+    expert = synth.expert_nbytes(s)
+    Lyr = shape.n_layers
+    routed = Lyr * s.K * expert
+    shared = Lyr * expert if shape.shared_expert else 0
+    r = shape.lora_rank
+    lora = Lyr * 2 * r * (2 * (s.H + s.I) + (s.I + s.H)) if shape.shared_expert else 0
+    hid = shape.head_hidden
+    head = (hid * s.H * 2 + s.E * s.H * 2 + s.E * hid * 2 + 2 * s.K * (hid + s.E) * 2 + (hid + s.E) * 2)
+    heads = len(shape.owners) * head
+    routers = native_layers * s.E * s.H * 2
+    return {"routed": routed, "shared": shared, "lora": lora, "heads": heads, "routers": routers,
+            "total": routed + shared + lora + heads + routers}
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[2]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "int4_gathered_expert_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    except (OSError, ValueError):
+        return None
+    k = rec.get(kernel)
+    if not k or k.get("source_digest") != kernel_source_digest():
+        return None
+    return k.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+
+def time_oracle(model, n_tokens: int):
+    """The oracle as it stands, decoding the first ``n_tokens`` of the stream."""
+    from oracle import e0_oracle as O
+    st = O.StackState(len(model.banks))
+    t0 = time.perf_counter()
+    for t in range(n_tokens):
+        O.stack_token(model.x[t], model, st)
+    return time.perf_counter() - t0
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- arms
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from int4_gathered_expert_gb300 import synth
+    shape = synth.STACK35B
+    n = args.warmup + args.steps
+    model = synth.stack_model(shape, n_tokens=max(n, 2))
+    # each step: one decode token of the same workload through all 40 layers
+    from oracle import e0_oracle as O
+    st = O.StackState(shape.n_layers)
+    for t in range(args.warmup):
+        O.stack_token(model.x[t], model, st)
+    t0 = time.perf_counter()
+    for t in range(args.warmup, n):
+        O.stack_token(model.x[t], model, st)
+    el = time.perf_counter() - t0
+    v = args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step": 1, "sample": "one decode token per step"},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": cores(), "kind": "oracle",
+                             "sample": f"{args.steps} decode tokens (after {args.warmup} warm-up tokens) of the "
+                                       "40-layer stack, float64 numpy oracle"},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from int4_gathered_expert_gb300 import synth
+    from int4_gathered_expert_gb300.model import StackDev
+
+    shape = synth.STACK35B
+    tps = args.tokens_per_step
+    n_tok = (args.warmup + args.steps) * tps
+    model = synth.stack_model(shape, n_tokens=n_tok)
+    sd = StackDev(model, trace=False)
+    X = torch.from_numpy(model.x).to(dev)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def decode(t0, t1, ev=None):
+        with torch.cuda.stream(stream):
+            for t in range(t0, t1):
+                if ev is not None:
+                    ev[t - t0][0].record(stream)
+                sd.step(X[t], impl=args.kernel_impl, stream=stream)
+                if ev is not None:
+                    ev[t - t0][1].record(stream)
+
+    # warm-up (includes token 0, which routes every layer natively)
+    decode(0, args.warmup * tps)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+
+    clk = ClockSampler(dev)
+    clk.start()
+    n_timed = args.steps * tps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_timed)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    decode(args.warmup * tps, n_tok, ev)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    el_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    st = int(sd.status.cpu().item())
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([el_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        el_ms = float(tt.item())
+        dist.barrier()
+
+    value = ws * n_timed / (el_ms / 1e3)
+    nb = bytes_per_token(shape, native_layers=7)
+    mean_launch_s = float(np.mean(launch_ms)) / 1e3
+    pk = peaks()
+    peak = pk["hbm_gbs"] if pk else 6800.0
+    achieved = nb["total"] / mean_launch_s / 1e9
+    traffic = recorded_traffic("k_stack_token")
+
+    # end to end: the same decode through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        Xh = torch.from_numpy(model.x).pin_memory()
+        out_h = torch.empty((tps, shape.layer.H), dtype=torch.float32).pin_memory()
+        xin = torch.empty(shape.layer.H, dtype=torch.float32, device=dev)
+        rout = torch.empty(shape.layer.H, dtype=torch.float32, device=dev)
+        sd.prepare()
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        w0 = time.perf_counter()
+        for sstep in range(args.warmup + args.steps):
+            if sstep == args.warmup:
+                torch.cuda.synchronize()
+                w0 = time.perf_counter()
+            with torch.cuda.stream(stream):
+                for i in range(tps):
+                    t = sstep * tps + i
+                    xin.copy_(Xh[t], non_blocking=True)
+                    sd.step(xin, impl=args.kernel_impl, stream=stream, out=rout)
+                    out_h[i].copy_(rout, non_blocking=True)
+            stream.synchronize()
+        e2e_s = time.perf_counter() - w0
+        if ws > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        e2e = {"value": ws * n_timed / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": tps * shape.layer.H * 4,
+               "d2h_bytes_per_step": tps * shape.layer.H * 4}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        n_cpu = 2
+        el = time_oracle(model, n_cpu)
+        cpu = {"value": n_cpu / el, "unit": "tok/s", "cores": cores(), "kind": "oracle",
+               "sample": f"first {n_cpu} tokens of the same stream (token 0 routes all 40 layers natively) "
+                         "through the 40-layer stack, float64 numpy oracle"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "int4 x int16 dp4a -> int32, f32 epilogue",
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD, "tokens_per_step": tps, "batch": 1,
+                           "l2": "no flush: each token streams %.0f MB of weights, more than the 129 MB L2"
+                                 % (nb["total"] / 1e6),
+                           "kernel": "persistent cooperative kernel, one launch per token"
+                           if args.kernel_impl == 0 else "per-phase kernel chain"},
+                "expert_weight_gbs": value * nb["routed"] / 1e9 / ws if ws else None,
+                "weight_gbs": value * nb["total"] / 1e9 / ws if ws else None,
+                "bytes_per_token": nb,
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": traffic,
+                             "kernel": "k_stack_token", "launch_us": mean_launch_s * 1e6,
+                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback"},
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_timed * (1 if args.kernel_impl == 0 else 241),
+                "clocks": clocks, "device_status": st}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,318 @@
+/*
+ * e0moe.h — C ABI of the GB300 (sm_103a) int4 gathered-expert MoE block, the
+ * decode/prefill hot path of the Edge0 streaming-MoE engine.
+ *
+ * Sources, cited by page title and section:
+ *   [KOALA]  "Edge0: 35B MoE를 SSD에서 3GiB 메모리로 서빙하기 — 라우팅을 한 토큰
+ *            먼저 예측한다" (koala.ai.kr).
+ *   [PTKR]   "edge0: 35B MoE 모델을 활성 메모리 3GiB로 실행하는 SSD 전문가
+ *            스트리밍 추론 프레임워크" (discuss.pytorch.kr).
+ *   [JAEHUN] "The Other Half of the Memory Wall: Serving 35B MoEs from SSD with
+ *            Trained Routing Prediction" (jaehun.me review; cites paper sections).
+ *   [XYZNOT] same title (xyznot.com summary).
+ *
+ * Conventions for every entry point
+ *   - Pointers named d_* or documented "device" are device pointers owned by
+ *     the caller; the library never frees or keeps them.  Pointers documented
+ *     "host" are read during the call only.
+ *   - fp16 data is passed as uint16_t (IEEE binary16 bits).
+ *   - Calls are asynchronous on the given stream (a cudaStream_t; NULL = the
+ *     legacy default stream) and never synchronise the host, except
+ *     e0_read_status, e0_stack_prepare and e0_pack_experts where stated.
+ *   - No call allocates memory.  Scratch comes from a caller workspace whose
+ *     size the matching *_workspace_size function reports; it needs 256-byte
+ *     alignment and its contents are not preserved across calls unless stated.
+ *   - Return value: E0_OK or a negative E0_ERR_* code.  Arguments are checked
+ *     on the host before anything is launched; a call that fails its checks
+ *     launches nothing.
+ *   - Conditions found on the device (a routed expert with no slot, an expert
+ *     id out of range, a non-finite logit, an exhausted wait) never trap: they
+ *     OR E0_ST_* bits into the caller's d_status word (when non-NULL) and the
+ *     affected contribution is zero.  e0_read_status copies the word back.
+ *
+ * Canonical int4 projection ("Q-tensor") for a matrix with `out` rows and `in`
+ * inputs — affine int4 with group size 64 along the input dimension ([KOALA]
+ * §1 "SSD 스트리밍 전문가 레이어" and the tier table "두 공개 티어"; [PTKR]
+ * "SSD 전문가 스트리밍"):
+ *     codes  uint8  [out][in/2]   element j of a row: byte j/2, low nibble when
+ *                                 j is even, high nibble when j is odd (q 0..15)
+ *     scale  fp16   [out][in/64]
+ *     bias   fp16   [out][in/64]
+ *     w[o][j] = scale[o][j/64] * q[o][j] + bias[o][j/64]
+ * An expert is gate [I][H], up [I][H], down [H][I]; y = down(silu(gate x) *
+ * up x) ([JAEHUN] "새로운 접근법: Edge0", paper §3.1 math contract).
+ *
+ * Kernel ("slot") layout of one expert, produced by e0_pack_experts, in
+ * e0_slot_bytes(H, I) bytes:
+ *     [0, I*H)                 gate/up codes, row-interleaved: for each i the
+ *                              gate row i (H/2 bytes) then the up row i
+ *     [I*H, I*H + H*I/2)       down codes, [H][I/2]
+ *     next I*(H/64)*2*4 bytes  gate/up (scale, bias) fp16 pairs, [I][2][H/64]
+ *     next H*(I/64)*4 bytes    down (scale, bias) fp16 pairs, [H][I/64]
+ * Codes keep the canonical row order, but inside every 32-bit word (8
+ * elements e0..e7 of a row) the nibbles are interleaved: nibble j (bits
+ * 4j..4j+3, little-endian word) holds e0, e2, e4, e6, e1, e3, e5, e7 for
+ * j = 0..7.  Masking a word with 0x000F000F / 0x00F000F0 (and the same after
+ * a shift by 8) then yields consecutive element pairs, and masking with
+ * 0x0F0F0F0F yields four byte lanes.  H and I must be multiples of 64 and at
+ * most 2048.
+ */
+#ifndef E0MOE_H
+#define E0MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* e0_stream_t; /* the same handle as cudaStream_t */
+
+/* ---- return codes ---------------------------------------------------- */
+enum {
+    E0_OK = 0,
+    E0_ERR_ARG = -1,         /* a shape, size or option is invalid          */
+    E0_ERR_NULL = -2,        /* a required pointer is NULL                  */
+    E0_ERR_UNSUPPORTED = -3, /* valid but outside what the kernels support  */
+    E0_ERR_CUDA = -4         /* a CUDA launch or copy returned an error     */
+};
+
+/* ---- device status bits (OR-ed into *d_status) ------------------------ */
+enum {
+    E0_ST_SLOT_MISS = 1u,    /* a routed expert has no slot: contributes 0  */
+    E0_ST_BAD_EXPERT = 2u,   /* an expert id outside [0, E): ignored        */
+    E0_ST_NONFINITE = 4u,    /* a routing score was NaN or infinite         */
+    E0_ST_TIMEOUT = 8u,      /* a bounded device-side wait gave up          */
+    E0_ST_POOL_FULL = 16u    /* slot_update found no free slot              */
+};
+
+/* ---- routing rules -------------------------------------------------- */
+enum { E0_ROUTE_SOFTMAX_TOPK = 0, E0_ROUTE_SIGMOID_GROUP = 1 };
+
+/* Limits of the kernels (E0_ERR_UNSUPPORTED beyond them). */
+enum { E0_MAX_E = 1024, E0_MAX_K = 32, E0_MAX_T_DECODE = 64, E0_MAX_LORA_RANK = 64 };
+
+typedef struct e0_qtensor {
+    const uint8_t* codes;    /* device, [out][in/2]  */
+    const uint16_t* scale;   /* device, fp16 [out][in/64] */
+    const uint16_t* bias;    /* device, fp16 [out][in/64] */
+} e0_qtensor;
+
+typedef struct e0_expert_q {
+    e0_qtensor gate, up, down;
+} e0_expert_q;
+
+/* A slot pool: n_slots experts in the kernel layout plus the slot table that
+ * maps an expert id to its slot ([KOALA] §1 staged path; [JAEHUN] paper §3.1:
+ * routing indices reach the slots through a table, so they never leave the
+ * GPU).  A resident bank is a pool with n_slots == E and the identity table. */
+typedef struct e0_slot_pool {
+    uint8_t* data;           /* device, n_slots * e0_slot_bytes(H, I) bytes  */
+    int32_t* slot_table;     /* device [E]: expert -> slot, -1 = absent      */
+    int32_t* occupant;       /* device [n_slots]: slot -> expert, -1 = empty */
+    int32_t n_slots, H, I, E;
+} e0_slot_pool;
+
+typedef struct e0_route_params {
+    int32_t mode;            /* E0_ROUTE_SOFTMAX_TOPK or E0_ROUTE_SIGMOID_GROUP */
+    int32_t K;               /* experts per token, 1 <= K <= min(E, 32)         */
+    int32_t n_groups;        /* sigmoid-group: n, E % n == 0                    */
+    int32_t topk_groups;     /* sigmoid-group: G, 1 <= G <= n                   */
+    float scale;             /* sigmoid-group: s                                */
+    const float* logit_bias; /* device [E] added to router logits, or NULL      */
+} e0_route_params;
+
+/* Shared expert: one expert in the kernel layout plus an optional unmerged
+ * LoRA on each projection, P(x) = W_int4 x + (alpha/rank) B (A x)
+ * ([XYZNOT] "Ausführung des unzusammengeführten Adapters"; [KOALA] §3).
+ * A_* fp16 [rank][in], B_* fp16 [out][rank]; all six NULL = no LoRA. */
+typedef struct e0_shared_expert {
+    const uint8_t* data;     /* device, e0_slot_bytes(H, I) bytes, kernel layout */
+    const uint16_t* A_gate; const uint16_t* B_gate;
+    const uint16_t* A_up;   const uint16_t* B_up;
+    const uint16_t* A_down; const uint16_t* B_down;
+    int32_t rank;
+    float alpha;
+} e0_shared_expert;
+
+/* Prerouter head owned by layer N, predicting layer N+1 at token t+1
+ * ([XYZNOT] "Architektur des Prerouter-Heads": head(f) = fc2(gelu_erf(fc1 f))
+ * + l(f), f = [h ; onehot(top-K now) ; onehot(top-K previous token)],
+ * dim = H + 2E).  fp16 weights: fc1 [hidden][H+2E], b1 [hidden] or NULL,
+ * fc2 [E][hidden], b2 [E] or NULL, lres [E][H+2E] (the linear residual). */
+typedef struct e0_prerouter {
+    const uint16_t* fc1; const uint16_t* b1;
+    const uint16_t* fc2; const uint16_t* b2;
+    const uint16_t* lres;
+    int32_t H, E, hidden;
+} e0_prerouter;
+
+/* ---- sizes ------------------------------------------------------------ */
+
+/* Bytes of one expert in the kernel layout (equal to the canonical size). */
+size_t e0_slot_bytes(int H, int I);
+
+/* Workspace for e0_moe_block_forward / e0_prerouter_forward /
+ * e0_moe_prefill_forward.  op: 0 = moe_block_forward, 1 = prerouter_forward,
+ * 2 = moe_prefill_forward.  For op 1, I is read as the head's hidden width. */
+size_t e0_workspace_size(int op, int T, int H, int I, int E, int K);
+
+/* ---- packing and the slot table --------------------------------------- */
+
+/* Convert n experts from the canonical layout into pool slots: src[i] (host
+ * array of device descriptors) goes to slot dst_slots[i] (host array).  When
+ * expert_ids (host [n]) is non-NULL, also sets slot_table[expert_ids[i]] =
+ * dst_slots[i] and occupant[dst_slots[i]] = expert_ids[i] on the device.
+ * Not a hot-path call: it launches one kernel per expert and synchronises the
+ * stream before returning (the host arrays may be freed afterwards). */
+int e0_pack_experts(const e0_expert_q* src, int n, const e0_slot_pool* dst,
+                    const int32_t* dst_slots, const int32_t* expert_ids, e0_stream_t stream);
+
+/* Incremental in-place slot update (incr_stack: [KOALA] §1 staged path and
+ * 한계; [JAEHUN] paper §3.1 and Appx.B; [XYZNOT] "incremental sticky-slot
+ * stack").  For the next set d_inds_next [n_next] (device), copies every
+ * expert that has no slot from `bank` (device or host-mapped memory holding
+ * all E experts in the kernel layout, expert e at bank + e*e0_slot_bytes) into
+ * the lowest-numbered free slot, then updates slot_table and occupant.  A slot
+ * is free when it holds no expert of d_inds_cur [n_cur] (may be NULL) nor of
+ * the next set.  Only changed slots are written; a resident bank (every
+ * expert already has a slot) moves zero bytes.  No free slot left: sets
+ * E0_ST_POOL_FULL and leaves that expert absent.  Ids outside [0, E) set
+ * E0_ST_BAD_EXPERT and are skipped.  Single-block kernel; bytes move with
+ * 16-byte copies by all of its threads. */
+int e0_slot_update(const e0_slot_pool* pool, const int32_t* d_inds_next, int n_next,
+                   const int32_t* d_inds_cur, int n_cur, const uint8_t* bank,
+                   uint32_t* d_status, e0_stream_t stream);
+
+/* ---- routing (softmax-top-k and sigmoid group-limited top-k) ---------- */
+
+/* Softmax-top-k ([JAEHUN] "새로운 접근법: Edge0", paper Appx.A):
+ * g = softmax(l); inds = top-k(g, K); w = g[inds] / sum(g[inds]).
+ * logits fp32 [T][E] device; inds int32 [T][K] (descending score, ties to the
+ * lower expert id); w fp32 [T][K].  One warp per token. */
+int e0_route_softmax_topk(const float* logits, int T, int E, int K, int32_t* inds, float* w,
+                          uint32_t* d_status, e0_stream_t stream);
+
+/* Sigmoid group-limited top-k (same passage): sigma = sigmoid(l); groups are
+ * n contiguous blocks of E/n experts; a group's score is the sum of its two
+ * largest sigma; the best G groups are kept (ties to the lower group); inds =
+ * top-k(sigma, K) over kept groups; w = s*sigma[inds]/(sum sigma[inds] + 1e-20).
+ * Requires K <= G*E/n. */
+int e0_route_sigmoid_group(const float* logits, int T, int E, int n_groups, int topk_groups,
+                           int K, float s, int32_t* inds, float* w, uint32_t* d_status,
+                           e0_stream_t stream);
+
+/* h = r / sqrt(mean(r^2) + eps), no learned weight (the post-attention norm
+ * whose output feeds the MoE block and the head; [KOALA] §2).  fp32 [T][H]. */
+int e0_rmsnorm(const float* r, int T, int H, float eps, float* h, e0_stream_t stream);
+
+/* ---- decode MoE block ------------------------------------------------- */
+
+/* y = sum_k w_k * expert_{inds_k}(x) (+ shared(x)) for T decode tokens
+ * ([JAEHUN] paper §3.1 math contract and Appx.A; [KOALA] §2 prediction as
+ * routing).  x fp32 [T][H] device (the MoE input h).  Experts are read in
+ * place from `pool` through its slot table.
+ * Routing: when inds_in is NULL the block routes natively: logits = W_router
+ * x (+ rp->logit_bias), W_router fp16 [E][H], then rp's rule.  When inds_in
+ * (int32 [T][K]) and w_in (fp32 [T][K]) are given, that routing is used as is
+ * (a prediction made one token earlier); W_router may then be NULL.
+ * inds_out / w_out (may be NULL) receive the routing used.  shared may be
+ * NULL.  Output y fp32 [T][H].  T <= 64. */
+int e0_moe_block_forward(const float* x, int T, const e0_slot_pool* pool,
+                         const uint16_t* W_router, const e0_route_params* rp,
+                         const int32_t* inds_in, const float* w_in,
+                         const e0_shared_expert* shared,
+                         float* y, int32_t* inds_out, float* w_out,
+                         void* ws, size_t ws_bytes, uint32_t* d_status, e0_stream_t stream);
+
+/* Prerouter head for T tokens: z = fc2 gelu_erf(fc1 f + b1) + b2 + lres f with
+ * f = [h ; onehot(inds_cur) ; onehot(inds_prev)] (inds_prev NULL = all zeros,
+ * the first token), then rp's routing of z gives the next layer's routing for
+ * the next token ([PTKR] "라우팅을 한 스텝 먼저 예측하는 프리라우터"; [JAEHUN]
+ * "작동 원리" toy example).  h fp32 [T][H]; inds_cur/inds_prev int32 [T][K];
+ * logits_out fp32 [T][E] (may be NULL); inds_next [T][K]; w_next [T][K]. */
+int e0_prerouter_forward(const float* h, int T, const int32_t* inds_cur, const int32_t* inds_prev,
+                         const e0_prerouter* head, const e0_route_params* rp,
+                         float* logits_out, int32_t* inds_next, float* w_next,
+                         void* ws, size_t ws_bytes, uint32_t* d_status, e0_stream_t stream);
+
+/* ---- decode stack (one token through L layers) ----------------------- */
+
+/* One layer of a decode stack.  `pool` holds the layer's experts (normally
+ * the resident bank); W_router fp16 [E][H] routes the layer natively (every
+ * layer at the first token, non-consumers always); `consumer` = 1 makes the
+ * layer route with the prediction its owner made one token earlier once one
+ * exists; `head` (or NULL) is the prerouter this layer owns; `shared` may be
+ * NULL.  The descriptors pointed to are copied by e0_stack_prepare. */
+typedef struct e0_stack_layer {
+    e0_slot_pool pool;
+    const uint16_t* W_router;
+    const e0_shared_expert* shared;
+    const e0_prerouter* head;
+    int32_t consumer;
+} e0_stack_layer;
+
+/* Optional per-token trace (device buffers; any may be NULL):
+ * r [L+1][H] residual stream at every layer input and the output,
+ * inds/w [L][K] the routing each layer used, head_logits [L][E] the logits of
+ * the head each owner evaluated (rows of non-owners untouched),
+ * pred_inds [L][K] the routing predicted for each consumer for the next token. */
+typedef struct e0_stack_trace {
+    float* r;
+    int32_t* inds;
+    float* w;
+    float* head_logits;
+    int32_t* pred_inds;
+} e0_stack_trace;
+
+/* Workspace of a stack (state carried between tokens lives here). */
+size_t e0_stack_workspace_size(int L, int H, int I, int E, int K, int head_hidden);
+
+/* Copy the layer descriptors into the workspace and clear the routing
+ * history (the next step is token 0).  Synchronises the stream. */
+int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
+                     const e0_route_params* rp, void* ws, size_t ws_bytes, e0_stream_t stream);
+
+/* Decode one token: r_0 = x; for each layer h = rmsnorm(r) (eps 1e-6);
+ * route (prediction or native); r += MoE(h) + Shared(h); owners evaluate their
+ * head and store the next token's routing for layer+1.  x fp32 [H] device,
+ * r_out fp32 [H] device.  impl: 0 = one persistent cooperative kernel for the
+ * whole token, 1 = a chain of per-phase kernels (same arithmetic). */
+int e0_stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* trace,
+                  int impl, uint32_t* d_status, e0_stream_t stream);
+
+/* ---- whole-layer prefill (sorted gather + tcgen05 grouped GEMM) ------- */
+
+/* Group the T*K assignments (t, k) by expert ([PTKR] "SSD 전문가 스트리밍":
+ * the full-layer path computes with a sorted gather).  counts [E], offsets
+ * [E+1] (exclusive scan), perm [T*K]: assignment ids t*K+k ordered by expert,
+ * token order kept within an expert. */
+int e0_prefill_sort(const int32_t* inds, int T, int K, int E, int32_t* counts, int32_t* offsets,
+                    int32_t* perm, void* ws, size_t ws_bytes, e0_stream_t stream);
+
+/* Prefill one layer for T tokens: route every token natively (logits =
+ * W_router X + rp->logit_bias), sort assignments by expert, gather X rows,
+ * run gate/up and down as grouped GEMMs on the tensor cores (fp16 operands,
+ * weights dequantised on chip, fp32 accumulation), and combine Y[t] =
+ * sum_k w[t][k] expert(X[t]) in a fixed order.  X fp16 [T][H]; bank = the
+ * layer's experts (slot table consulted per expert); Y fp32 [T][H];
+ * inds_out/w_out [T][K].  Prefill never predicts ([JAEHUN] "작동 원리"). */
+int e0_moe_prefill_forward(const uint16_t* X, int T, const e0_slot_pool* bank,
+                           const uint16_t* W_router, const e0_route_params* rp,
+                           float* Y, int32_t* inds_out, float* w_out,
+                           void* ws, size_t ws_bytes, uint32_t* d_status, e0_stream_t stream);
+
+/* ---- status ------------------------------------------------------------- */
+
+/* Copy *d_status to *h_out after everything queued on `stream`; synchronises
+ * the stream. */
+int e0_read_status(const uint32_t* d_status, uint32_t* h_out, e0_stream_t stream);
+
+/* A static string describing a return code. */
+const char* e0_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* E0MOE_H */

@@ -1,0 +1,923 @@
+// Decode path of the int4 gathered-expert MoE block: kernels and the C entry
+// points for packing, slot update, routing, RMSNorm, the MoE block, the
+// prerouter head and the whole-token decode stack.
+#include <stdio.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+
+#include "e0_decode.cuh"
+#include "e0_internal.h"
+
+namespace e0 {
+
+constexpr int PHASE_THREADS = 256;
+constexpr uint32_t BARRIER_SPIN_LIMIT = 1u << 22;
+
+// ================================================================== packing
+
+__global__ void k_pack_expert(e0_expert_q src, uint8_t* dst, int H, int I, int32_t* table, int32_t* occupant,
+                              int eid, int slot) {
+    const SlotLayout sl{H, I};
+    const int GH = H / GROUP, GI = I / GROUP;
+    const size_t n_gu = (size_t)I * H / 16;            // 16-byte chunks of gate/up codes
+    const size_t n_dn = (size_t)H * I / 2 / 16;        // down codes
+    const size_t n_gsb = (size_t)I * GH * 2;           // gate/up scale-bias pairs
+    const size_t n_dsb = (size_t)H * GI;               // down scale-bias pairs
+    const size_t total = n_gu + n_dn + n_gsb + n_dsb;
+    const size_t row16 = (size_t)H / 16;               // chunks per interleaved gate+up row
+    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (size_t)gridDim.x * blockDim.x) {
+        if (q < n_gu) {
+            const size_t i = q / row16, c = q % row16;
+            const size_t half = row16 / 2;
+            const uint8_t* s = c < half ? src.gate.codes + i * (H / 2) + c * 16 : src.up.codes + i * (H / 2) + (c - half) * 16;
+            *reinterpret_cast<uint4*>(dst + i * H + c * 16) = interleave16(*reinterpret_cast<const uint4*>(s));
+        } else if (q < n_gu + n_dn) {
+            const size_t c = q - n_gu;
+            *reinterpret_cast<uint4*>(dst + sl.down_codes() + c * 16) =
+                interleave16(*reinterpret_cast<const uint4*>(src.down.codes + c * 16));
+        } else if (q < n_gu + n_dn + n_gsb) {
+            const size_t p = q - n_gu - n_dn;
+            const size_t i = p / (2 * GH), which = (p / GH) % 2, g = p % GH;
+            const e0_qtensor& qt = which ? src.up : src.gate;
+            const uint32_t v = (uint32_t)qt.scale[i * GH + g] | ((uint32_t)qt.bias[i * GH + g] << 16);
+            *reinterpret_cast<uint32_t*>(dst + sl.gu_sb() + p * 4) = v;
+        } else {
+            const size_t p = q - n_gu - n_dn - n_gsb;
+            const uint32_t v = (uint32_t)src.down.scale[p] | ((uint32_t)src.down.bias[p] << 16);
+            *reinterpret_cast<uint32_t*>(dst + sl.down_sb() + p * 4) = v;
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && table != nullptr && eid >= 0) {
+        table[eid] = slot;
+        if (occupant) occupant[slot] = eid;
+    }
+}
+
+// ================================================================== slot update
+
+struct SlotPlan {
+    int n;
+    int e[E0_MAX_T_DECODE * E0_MAX_K];
+    int s[E0_MAX_T_DECODE * E0_MAX_K];
+    uint32_t status;
+};
+
+// Single thread: the copies that bring every expert of `next` into the pool.
+E0_DEV void slot_plan(const int32_t* table, const int32_t* occupant, int n_slots, int E, const int32_t* next,
+                      int n_next, const int32_t* cur, int n_cur, SlotPlan* P, uint32_t* prot /*(n_slots+31)/32*/) {
+    const int nw = (n_slots + 31) / 32;
+    for (int i = 0; i < nw; ++i) prot[i] = 0;
+    P->n = 0;
+    P->status = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int32_t* v = pass ? cur : next;
+        const int nv = pass ? n_cur : n_next;
+        for (int i = 0; v && i < nv; ++i) {
+            const int e = v[i];
+            if (e < 0 || e >= E) continue;
+            const int s = table[e];
+            if (s >= 0 && s < n_slots) prot[s >> 5] |= 1u << (s & 31);
+        }
+    }
+    int cursor = 0;
+    for (int i = 0; i < n_next; ++i) {
+        const int e = next[i];
+        if (e < 0 || e >= E) {
+            P->status |= E0_ST_BAD_EXPERT;
+            continue;
+        }
+        bool dup = false;
+        for (int j = 0; j < i; ++j) dup |= next[j] == e;
+        if (dup || table[e] >= 0) continue;
+        while (cursor < n_slots && ((prot[cursor >> 5] >> (cursor & 31)) & 1u)) ++cursor;
+        if (cursor >= n_slots) {
+            P->status |= E0_ST_POOL_FULL;
+            continue;
+        }
+        prot[cursor >> 5] |= 1u << (cursor & 31);
+        P->e[P->n] = e;
+        P->s[P->n] = cursor;
+        P->n++;
+    }
+    (void)occupant;
+}
+
+__global__ void k_slot_copy(const int32_t* table, const int32_t* occupant, uint8_t* pool, int n_slots, int E,
+                            const int32_t* next, int n_next, const int32_t* cur, int n_cur, const uint8_t* bank,
+                            size_t sbytes) {
+    __shared__ SlotPlan P;
+    __shared__ uint32_t prot[E0_MAX_E / 32];
+    if (threadIdx.x == 0) slot_plan(table, occupant, n_slots, E, next, n_next, cur, n_cur, &P, prot);
+    __syncthreads();
+    const size_t chunks = sbytes / 16;
+    const size_t total = chunks * P.n;
+    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(q / chunks);
+        const size_t off = (q % chunks) * 16;
+        const uint4 v = *reinterpret_cast<const uint4*>(bank + (size_t)P.e[c] * sbytes + off);
+        *reinterpret_cast<uint4*>(pool + (size_t)P.s[c] * sbytes + off) = v;
+    }
+}
+
+__global__ void k_slot_commit(int32_t* table, int32_t* occupant, int n_slots, int E, const int32_t* next, int n_next,
+                              const int32_t* cur, int n_cur, uint32_t* st) {
+    __shared__ SlotPlan P;
+    __shared__ uint32_t prot[E0_MAX_E / 32];
+    if (threadIdx.x != 0) return;
+    slot_plan(table, occupant, n_slots, E, next, n_next, cur, n_cur, &P, prot);
+    for (int c = 0; c < P.n; ++c) {
+        const int s = P.s[c], e = P.e[c];
+        const int old = occupant[s];
+        if (old >= 0 && old < E && table[old] == s) table[old] = -1;
+        occupant[s] = e;
+        table[e] = s;
+    }
+    if (P.status) set_status(st, P.status);
+}
+
+// ================================================================== routing / norm
+
+__global__ void k_route(const float* logits, int T, int E, RouteP rp, int32_t* inds, float* w, uint32_t* st) {
+    extern __shared__ float scr[];  // E floats per warp
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (t >= T) return;
+    route_warp(logits + (size_t)t * E, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr + warp * E, st,
+               lane);
+}
+
+__global__ void k_rmsnorm(const float* r, int H, float eps, float* h) {
+    __shared__ float red[32];
+    rmsnorm_block(r + (size_t)blockIdx.x * H, h + (size_t)blockIdx.x * H, H, eps, red);
+}
+
+// ================================================================== phase kernels
+
+__global__ void __launch_bounds__(PHASE_THREADS) k_router(DecodeArgs A) { phase_router(A, blockIdx.x, gridDim.x); }
+
+__global__ void __launch_bounds__(PHASE_THREADS) k_gateup(DecodeArgs A) {
+    extern __shared__ __align__(16) char smem[];
+    phase_gateup(A, A.inds, blockIdx.x, gridDim.x, smem);
+}
+
+__global__ void __launch_bounds__(PHASE_THREADS) k_down(DecodeArgs A) {
+    extern __shared__ __align__(16) char smem[];
+    phase_down(A, blockIdx.x, gridDim.x, smem);
+}
+
+// ================================================================== stack
+
+struct StackHdr {
+    int32_t L, H, I, E, K, hidden, rank;
+    RouteP rp;
+    int32_t t;
+    uint32_t bar_count, bar_gen, bar_abort;
+    LayerP* layers;
+    int32_t* hist;       // [2][L][K]
+    float* wcur;         // [L][K]
+    int32_t* pred_inds;  // [2][L][K]
+    float* pred_w;       // [2][L][K]
+    float* r;            // [H]
+    float* h;            // [H]
+    float* logits;       // [E]
+    float* a;            // [K][I]
+    float* gs;           // [I]
+    float* us;           // [I]
+    float* zg;           // [rank]
+    float* zu;           // [rank]
+    float* hpre;         // [hidden]
+    float* zres;         // [E]
+    float* z;            // [E]
+    int32_t grid;        // blocks of the persistent kernel
+    int32_t smem;        // its dynamic shared memory
+};
+
+struct TraceP {
+    float* r;
+    int32_t* inds;
+    float* w;
+    float* head_logits;
+    int32_t* pred_inds;
+};
+
+struct WsCarve {
+    char* base;
+    size_t off;
+    template <class T>
+    T* take(size_t n) {
+        off = (off + 255) & ~(size_t)255;
+        T* p = reinterpret_cast<T*>(base + off);
+        off += n * sizeof(T);
+        return p;
+    }
+};
+
+static size_t stack_layout(StackHdr* hdr, char* base, int L, int H, int I, int E, int K, int hidden, int rank) {
+    WsCarve c{base, 0};
+    c.take<StackHdr>(1);
+    LayerP* layers = c.take<LayerP>(L);
+    int32_t* hist = c.take<int32_t>((size_t)2 * L * K);
+    float* wcur = c.take<float>((size_t)L * K);
+    int32_t* pi = c.take<int32_t>((size_t)2 * L * K);
+    float* pw = c.take<float>((size_t)2 * L * K);
+    float* r = c.take<float>(H);
+    float* h = c.take<float>(H);
+    float* lg = c.take<float>(E);
+    float* a = c.take<float>((size_t)K * I);
+    float* gs = c.take<float>(I);
+    float* us = c.take<float>(I);
+    float* zg = c.take<float>(rank > 0 ? rank : 1);
+    float* zu = c.take<float>(rank > 0 ? rank : 1);
+    float* hp = c.take<float>(hidden > 0 ? hidden : 1);
+    float* zr = c.take<float>(E);
+    float* z = c.take<float>(E);
+    if (hdr) {
+        hdr->layers = layers;
+        hdr->hist = hist;
+        hdr->wcur = wcur;
+        hdr->pred_inds = pi;
+        hdr->pred_w = pw;
+        hdr->r = r;
+        hdr->h = h;
+        hdr->logits = lg;
+        hdr->a = a;
+        hdr->gs = gs;
+        hdr->us = us;
+        hdr->zg = zg;
+        hdr->zu = zu;
+        hdr->hpre = hp;
+        hdr->zres = zr;
+        hdr->z = z;
+    }
+    return c.off + 256;
+}
+
+E0_DEV DecodeArgs stack_args(const StackHdr& S, const LayerP& L, const float* h, const float* resid, float* y,
+                             const int32_t* inds, const float* w, const int32_t* inds_prev, uint32_t* st) {
+    DecodeArgs A;
+    A.T = 1;
+    A.H = S.H;
+    A.I = S.I;
+    A.E = S.E;
+    A.K = S.K;
+    A.x = h;
+    A.resid = resid;
+    A.inds = inds;
+    A.w = w;
+    A.inds_prev = inds_prev;
+    A.L = L;
+    A.a = S.a;
+    A.gs = S.gs;
+    A.us = S.us;
+    A.zg = S.zg;
+    A.zu = S.zu;
+    A.hpre = S.hpre;
+    A.zres = S.zres;
+    A.y = y;
+    A.z = L.fc1 ? S.z : nullptr;
+    A.logits = S.logits;
+    A.st = st;
+    return A;
+}
+
+E0_DEV bool layer_native(const StackHdr& S, const LayerP& L, int t) { return t == 0 || !L.consumer; }
+
+// Route the head logits z of owner layer `l` into the prediction consumed by
+// layer l+1 at the next token (one warp).
+E0_DEV void stack_route_head(const StackHdr& S, int l, int t, float* scr, TraceP tr, uint32_t* st, int lane) {
+    if (l + 1 >= S.L) return;
+    const int np = (t + 1) & 1;
+    int32_t* pi = S.pred_inds + ((size_t)np * S.L + (l + 1)) * S.K;
+    float* pw = S.pred_w + ((size_t)np * S.L + (l + 1)) * S.K;
+    RouteP rp = S.rp;
+    rp.logit_bias = nullptr;
+    route_warp(S.z, S.E, rp, pi, pw, scr, st, lane);
+    __syncwarp();
+    if (tr.head_logits)
+        for (int e = lane; e < S.E; e += 32) tr.head_logits[(size_t)l * S.E + e] = __ldcg(S.z + e);
+    if (tr.pred_inds && lane < S.K) tr.pred_inds[(size_t)(l + 1) * S.K + lane] = pi[lane];
+}
+
+// Resolve the routing layer l uses at token t into inds/w (one warp).
+E0_DEV void stack_resolve(const StackHdr& S, const LayerP& L, int l, int t, int32_t* inds, float* w, float* scr,
+                          uint32_t* st, int lane) {
+    if (layer_native(S, L, t)) {
+        route_warp(S.logits, S.E, S.rp, inds, w, scr, st, lane);
+    } else if (lane < S.K) {
+        const size_t o = ((size_t)(t & 1) * S.L + l) * S.K + lane;
+        inds[lane] = __ldcg(S.pred_inds + o);
+        w[lane] = __ldcg(S.pred_w + o);
+    }
+    __syncwarp();
+}
+
+// ---- chain implementation: one kernel per phase
+
+__global__ void k_stack_norm(StackHdr* Sp, int l, const float* x, TraceP tr) {
+    __shared__ float red[32];
+    const StackHdr& S = *Sp;
+    const float* rin = l == 0 ? x : S.r;
+    rmsnorm_block(rin, S.h, S.H, 1e-6f, red);
+    if (tr.r)
+        for (int j = threadIdx.x; j < S.H; j += blockDim.x) tr.r[(size_t)l * S.H + j] = rin[j];
+}
+
+__global__ void __launch_bounds__(PHASE_THREADS) k_stack_router(StackHdr* Sp, int l, uint32_t* st) {
+    const StackHdr& S = *Sp;
+    const LayerP& L = S.layers[l];
+    if (!layer_native(S, L, S.t)) return;
+    DecodeArgs A = stack_args(S, L, S.h, nullptr, nullptr, nullptr, nullptr, nullptr, st);
+    phase_router(A, blockIdx.x, gridDim.x);
+}
+
+__global__ void k_stack_resolve(StackHdr* Sp, int l, TraceP tr, uint32_t* st) {
+    extern __shared__ float scr[];
+    const StackHdr& S = *Sp;
+    const int t = S.t, lane = threadIdx.x & 31;
+    int32_t* inds = S.hist + ((size_t)(t & 1) * S.L + l) * S.K;
+    float* w = S.wcur + (size_t)l * S.K;
+    stack_resolve(S, S.layers[l], l, t, inds, w, scr, st, lane);
+    if (lane < S.K) {
+        if (tr.inds) tr.inds[(size_t)l * S.K + lane] = inds[lane];
+        if (tr.w) tr.w[(size_t)l * S.K + lane] = w[lane];
+    }
+}
+
+__global__ void __launch_bounds__(PHASE_THREADS) k_stack_gateup(StackHdr* Sp, int l, uint32_t* st) {
+    extern __shared__ __align__(16) char smem[];
+    const StackHdr& S = *Sp;
+    const LayerP& L = S.layers[l];
+    const int t = S.t;
+    const int32_t* inds = S.hist + ((size_t)(t & 1) * S.L + l) * S.K;
+    const int32_t* prev = t > 0 ? S.hist + ((size_t)((t + 1) & 1) * S.L + l) * S.K : nullptr;
+    DecodeArgs A = stack_args(S, L, S.h, nullptr, nullptr, inds, S.wcur + (size_t)l * S.K, prev, st);
+    phase_gateup(A, inds, blockIdx.x, gridDim.x, smem);
+}
+
+__global__ void __launch_bounds__(PHASE_THREADS) k_stack_down(StackHdr* Sp, int l, const float* x, float* r_out,
+                                                              uint32_t* st) {
+    extern __shared__ __align__(16) char smem[];
+    const StackHdr& S = *Sp;
+    const LayerP& L = S.layers[l];
+    const int t = S.t;
+    const int32_t* inds = S.hist + ((size_t)(t & 1) * S.L + l) * S.K;
+    const float* rin = l == 0 ? x : S.r;
+    float* y = l == S.L - 1 ? r_out : S.r;
+    DecodeArgs A = stack_args(S, L, S.h, rin, y, inds, S.wcur + (size_t)l * S.K, nullptr, st);
+    phase_down(A, blockIdx.x, gridDim.x, smem);
+}
+
+__global__ void k_stack_head(StackHdr* Sp, int l, TraceP tr, uint32_t* st) {
+    extern __shared__ float scr[];
+    const StackHdr& S = *Sp;
+    if (!S.layers[l].fc1) return;
+    stack_route_head(S, l, S.t, scr, tr, st, threadIdx.x & 31);
+}
+
+__global__ void k_stack_finish(StackHdr* Sp, const float* r_out, TraceP tr) {
+    StackHdr& S = *Sp;
+    if (tr.r)
+        for (int j = threadIdx.x; j < S.H; j += blockDim.x) tr.r[(size_t)S.L * S.H + j] = r_out[j];
+    __syncthreads();
+    if (threadIdx.x == 0) S.t = S.t + 1;
+}
+
+// ---- persistent implementation: the whole token in one cooperative kernel
+
+E0_DEV void grid_barrier(StackHdr* S, uint32_t* st) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned gen;
+        asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(gen) : "l"(&S->bar_gen) : "memory");
+        __threadfence();
+        const unsigned arrived = atomicAdd(&S->bar_count, 1u);
+        if (arrived == gridDim.x - 1) {
+            atomicExch(&S->bar_count, 0u);
+            __threadfence();
+            asm volatile("st.release.gpu.u32 [%0], %1;" ::"l"(&S->bar_gen), "r"(gen + 1) : "memory");
+        } else {
+            uint32_t it = 0;
+            while (true) {
+                unsigned cur, ab;
+                asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(cur) : "l"(&S->bar_gen) : "memory");
+                if (cur != gen) break;
+                asm volatile("ld.relaxed.gpu.u32 %0, [%1];" : "=r"(ab) : "l"(&S->bar_abort) : "memory");
+                if (ab) break;
+                if (++it > BARRIER_SPIN_LIMIT) {
+                    set_status(st, E0_ST_TIMEOUT);
+                    atomicExch(&S->bar_abort, 1u);
+                    break;
+                }
+                if (it > 64) __nanosleep(32);
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+}
+
+struct PersistSmem {
+    size_t h, inds, w, scr, red, phase, total;
+    __host__ __device__ PersistSmem(int H, int E, int K, size_t phase_bytes) {
+        h = 0;
+        inds = h + (size_t)H * 4;
+        w = inds + 128;
+        scr = w + 128;
+        red = scr + (size_t)2 * E * 4;
+        phase = red + 128;
+        phase = (phase + 15) & ~(size_t)15;
+        total = phase + phase_bytes;
+        (void)K;
+    }
+};
+
+__global__ void __launch_bounds__(PHASE_THREADS) k_stack_token(StackHdr* Sp, const float* x, float* r_out, TraceP tr,
+                                                               uint32_t* st) {
+    extern __shared__ __align__(16) char smem[];
+    StackHdr& S = *Sp;
+    const int t = S.t;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t phase_bytes = (size_t)S.smem;
+    const PersistSmem lay(S.H, S.E, S.K, 0);
+    float* hbuf = reinterpret_cast<float*>(smem + lay.h);
+    int32_t* inds_s = reinterpret_cast<int32_t*>(smem + lay.inds);
+    float* w_s = reinterpret_cast<float*>(smem + lay.w);
+    float* scr = reinterpret_cast<float*>(smem + lay.scr);
+    float* red = reinterpret_cast<float*>(smem + lay.red);
+    char* psm = smem + lay.phase;
+    (void)phase_bytes;
+
+    for (int l = 0; l < S.L; ++l) {
+        const LayerP L = S.layers[l];
+        const bool native = layer_native(S, L, t);
+        const float* rin = l == 0 ? x : S.r;
+        // every block normalises the residual stream itself
+        {
+            float s = 0.f;
+            for (int j = threadIdx.x; j < S.H; j += blockDim.x) {
+                const float v = __ldcg(rin + j);
+                hbuf[j] = v;
+                s = fmaf(v, v, s);
+            }
+            s = warp_sum(s);
+            if (lane == 0) red[warp] = s;
+            __syncthreads();
+            if (warp == 0) {
+                float v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+                v = warp_sum(v);
+                if (lane == 0) red[0] = v;
+            }
+            __syncthreads();
+            const float denom = sqrtf(red[0] / (float)S.H + 1e-6f);
+            if (blockIdx.x == 0 && tr.r)
+                for (int j = threadIdx.x; j < S.H; j += blockDim.x) tr.r[(size_t)l * S.H + j] = hbuf[j];
+            __syncthreads();
+            for (int j = threadIdx.x; j < S.H; j += blockDim.x) hbuf[j] = hbuf[j] / denom;
+            __syncthreads();
+        }
+        if (native) {
+            DecodeArgs A = stack_args(S, L, hbuf, nullptr, nullptr, nullptr, nullptr, nullptr, st);
+            phase_router(A, blockIdx.x, gridDim.x);
+            grid_barrier(Sp, st);
+        }
+        // routing of this layer (every block, warp 0) and the previous owner's prediction (block 0, warp 1)
+        if (warp == 0) {
+            stack_resolve(S, L, l, t, inds_s, w_s, scr, blockIdx.x == 0 ? st : nullptr, lane);
+            if (blockIdx.x == 0 && lane < S.K) {
+                const size_t o = ((size_t)(t & 1) * S.L + l) * S.K + lane;
+                S.hist[o] = inds_s[lane];
+                S.wcur[(size_t)l * S.K + lane] = w_s[lane];
+                if (tr.inds) tr.inds[(size_t)l * S.K + lane] = inds_s[lane];
+                if (tr.w) tr.w[(size_t)l * S.K + lane] = w_s[lane];
+            }
+        } else if (warp == 1 && blockIdx.x == 0 && l > 0 && S.layers[l - 1].fc1) {
+            stack_route_head(S, l - 1, t, scr + S.E, tr, st, lane);
+        }
+        __syncthreads();
+        {
+            const int32_t* prev = t > 0 ? S.hist + ((size_t)((t + 1) & 1) * S.L + l) * S.K : nullptr;
+            DecodeArgs A = stack_args(S, L, hbuf, nullptr, nullptr, inds_s, w_s, prev, st);
+            phase_gateup(A, inds_s, blockIdx.x, gridDim.x, psm);
+        }
+        grid_barrier(Sp, st);
+        {
+            const int32_t* inds = S.hist + ((size_t)(t & 1) * S.L + l) * S.K;
+            float* y = l == S.L - 1 ? r_out : S.r;
+            DecodeArgs A = stack_args(S, L, hbuf, rin, y, inds, S.wcur + (size_t)l * S.K, nullptr, st);
+            phase_down(A, blockIdx.x, gridDim.x, psm);
+        }
+        grid_barrier(Sp, st);
+    }
+    if (blockIdx.x == 0) {
+        if (warp == 1 && S.layers[S.L - 1].fc1) stack_route_head(S, S.L - 1, t, scr + S.E, tr, st, lane);
+        if (tr.r)
+            for (int j = threadIdx.x; j < S.H; j += blockDim.x) tr.r[(size_t)S.L * S.H + j] = __ldcg(r_out + j);
+        __syncthreads();
+        if (threadIdx.x == 0) S.t = t + 1;
+    }
+}
+
+// ================================================================== host side
+
+static int g_num_sms = 0;
+static std::once_flag g_init;
+
+static void init_attrs() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    const int big = 200 * 1024;
+    cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    cudaFuncSetAttribute(k_stack_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    cudaFuncSetAttribute(k_stack_down, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    cudaFuncSetAttribute(k_stack_token, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+}
+
+int num_sms() {
+    std::call_once(g_init, init_attrs);
+    return g_num_sms > 0 ? g_num_sms : 148;
+}
+
+static int phase_grid(long warps) {
+    long blocks = (warps + (PHASE_THREADS / 32) - 1) / (PHASE_THREADS / 32);
+    const long cap = (long)num_sms() * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return (int)blocks;
+}
+
+static RouteP to_route(const e0_route_params* rp) {
+    RouteP r;
+    r.mode = rp->mode;
+    r.K = rp->K;
+    r.n_groups = rp->n_groups > 0 ? rp->n_groups : 1;
+    r.topk_groups = rp->topk_groups > 0 ? rp->topk_groups : 1;
+    r.scale = rp->scale;
+    r.logit_bias = rp->logit_bias;
+    return r;
+}
+
+static LayerP to_layer(const e0_slot_pool* pool, const uint16_t* W_r, const e0_shared_expert* sh,
+                       const e0_prerouter* head, int consumer) {
+    LayerP L;
+    memset(&L, 0, sizeof(L));
+    if (pool) {
+        L.pool = pool->data;
+        L.table = pool->slot_table;
+        L.n_slots = pool->n_slots;
+    }
+    L.W_r = reinterpret_cast<const __half*>(W_r);
+    if (sh) {
+        L.sh = sh->data;
+        if (sh->A_gate) {
+            L.Ag = reinterpret_cast<const __half*>(sh->A_gate);
+            L.Bg = reinterpret_cast<const __half*>(sh->B_gate);
+            L.Au = reinterpret_cast<const __half*>(sh->A_up);
+            L.Bu = reinterpret_cast<const __half*>(sh->B_up);
+            L.Ad = reinterpret_cast<const __half*>(sh->A_down);
+            L.Bd = reinterpret_cast<const __half*>(sh->B_down);
+            L.rank = sh->rank;
+            L.lscale = sh->alpha / (float)sh->rank;
+        }
+    }
+    if (head) {
+        L.fc1 = reinterpret_cast<const __half*>(head->fc1);
+        L.b1 = reinterpret_cast<const __half*>(head->b1);
+        L.fc2 = reinterpret_cast<const __half*>(head->fc2);
+        L.b2 = reinterpret_cast<const __half*>(head->b2);
+        L.lres = reinterpret_cast<const __half*>(head->lres);
+        L.hidden = head->hidden;
+    }
+    L.consumer = consumer;
+    return L;
+}
+
+static inline int cuda_ok(cudaError_t e) { return e == cudaSuccess ? E0_OK : E0_ERR_CUDA; }
+static inline int launch_ok() { return cuda_ok(cudaGetLastError()); }
+
+// ---- packing
+
+int pack_experts(const e0_expert_q* src, int n, const e0_slot_pool* dst, const int32_t* dst_slots,
+                 const int32_t* expert_ids, cudaStream_t s) {
+    num_sms();
+    const size_t sb = slot_bytes(dst->H, dst->I);
+    for (int i = 0; i < n; ++i) {
+        uint8_t* d = dst->data + (size_t)dst_slots[i] * sb;
+        k_pack_expert<<<num_sms() * 2, 256, 0, s>>>(src[i], d, dst->H, dst->I, dst->slot_table, dst->occupant,
+                                                     expert_ids ? expert_ids[i] : -1, dst_slots[i]);
+        if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+    }
+    return cuda_ok(cudaStreamSynchronize(s));
+}
+
+int slot_update(const e0_slot_pool* p, const int32_t* next, int n_next, const int32_t* cur, int n_cur,
+                const uint8_t* bank, uint32_t* st, cudaStream_t s) {
+    const size_t sb = slot_bytes(p->H, p->I);
+    k_slot_copy<<<num_sms(), 512, 0, s>>>(p->slot_table, p->occupant, p->data, p->n_slots, p->E, next, n_next, cur,
+                                          n_cur, bank, sb);
+    if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+    k_slot_commit<<<1, 32, 0, s>>>(p->slot_table, p->occupant, p->n_slots, p->E, next, n_next, cur, n_cur, st);
+    return launch_ok();
+}
+
+int route(const float* logits, int T, int E, const e0_route_params* rp, int32_t* inds, float* w, uint32_t* st,
+          cudaStream_t s) {
+    if (T == 0) return E0_OK;
+    const int wpb = 4;
+    k_route<<<(T + wpb - 1) / wpb, 32 * wpb, (size_t)wpb * E * sizeof(float), s>>>(logits, T, E, to_route(rp), inds,
+                                                                                   w, st);
+    return launch_ok();
+}
+
+int rmsnorm(const float* r, int T, int H, float eps, float* h, cudaStream_t s) {
+    if (T == 0) return E0_OK;
+    k_rmsnorm<<<T, 256, 0, s>>>(r, H, eps, h);
+    return launch_ok();
+}
+
+// ---- MoE block
+
+struct BlockWs {
+    float* logits;
+    int32_t* inds;
+    float* w;
+    float* a;
+    float* gs;
+    float* us;
+    float* zg;
+    float* zu;
+    float* hpre;
+    float* zres;
+    size_t bytes;
+};
+
+static BlockWs block_ws(char* base, int T, int H, int I, int E, int K, int rank, int hidden) {
+    const int Tc = T < 8 ? T : 8;
+    WsCarve c{base, 0};
+    BlockWs b;
+    b.logits = c.take<float>((size_t)T * E);
+    b.inds = c.take<int32_t>((size_t)T * K);
+    b.w = c.take<float>((size_t)T * K);
+    b.a = c.take<float>((size_t)Tc * K * I);
+    b.gs = c.take<float>((size_t)Tc * I);
+    b.us = c.take<float>((size_t)Tc * I);
+    b.zg = c.take<float>((size_t)Tc * (rank > 0 ? rank : 1));
+    b.zu = c.take<float>((size_t)Tc * (rank > 0 ? rank : 1));
+    b.hpre = c.take<float>((size_t)Tc * (hidden > 0 ? hidden : 1));
+    b.zres = c.take<float>((size_t)T * E);
+    b.bytes = c.off + 256;
+    (void)H;
+    return b;
+}
+
+size_t block_ws_bytes(int T, int H, int I, int E, int K, int rank, int hidden) {
+    return block_ws(nullptr, T, H, I, E, K, rank, hidden).bytes;
+}
+
+int moe_block_forward(const float* x, int T, const e0_slot_pool* pool, const uint16_t* W_r,
+                      const e0_route_params* rp, const int32_t* inds_in, const float* w_in,
+                      const e0_shared_expert* sh, float* y, int32_t* inds_out, float* w_out, void* ws,
+                      uint32_t* st, cudaStream_t s) {
+    num_sms();
+    const int H = pool->H, I = pool->I, E = pool->E, K = rp->K;
+    const int rank = (sh && sh->A_gate) ? sh->rank : 0;
+    BlockWs b = block_ws(reinterpret_cast<char*>(ws), T, H, I, E, K, 64, 0);
+    LayerP L = to_layer(pool, W_r, sh, nullptr, 0);
+    const int32_t* inds = inds_in;
+    const float* w = w_in;
+    if (!inds_in) {
+        DecodeArgs A;
+        memset(&A, 0, sizeof(A));
+        A.T = T;
+        A.H = H;
+        A.I = I;
+        A.E = E;
+        A.K = K;
+        A.x = x;
+        A.L = L;
+        A.logits = b.logits;
+        A.st = st;
+        const int R = (H / GROUP) >= 32 ? 1 : 32 / (H / GROUP);
+        const long warps = (long)T * ((E + R - 1) / R);
+        k_router<<<phase_grid(warps), PHASE_THREADS, 0, s>>>(A);
+        if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+        int32_t* io = inds_out ? inds_out : b.inds;
+        float* wo = w_out ? w_out : b.w;
+        int rc = route(b.logits, T, E, rp, io, wo, st, s);
+        if (rc) return rc;
+        inds = io;
+        w = wo;
+    } else {
+        if (inds_out && inds_out != inds_in &&
+            cudaMemcpyAsync(inds_out, inds_in, (size_t)T * K * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return E0_ERR_CUDA;
+        if (w_out && w_out != w_in &&
+            cudaMemcpyAsync(w_out, w_in, (size_t)T * K * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return E0_ERR_CUDA;
+    }
+    for (int t0 = 0; t0 < T; t0 += 8) {
+        const int Tc = T - t0 < 8 ? T - t0 : 8;
+        DecodeArgs A;
+        memset(&A, 0, sizeof(A));
+        A.T = Tc;
+        A.H = H;
+        A.I = I;
+        A.E = E;
+        A.K = K;
+        A.x = x + (size_t)t0 * H;
+        A.resid = nullptr;
+        A.inds = inds + (size_t)t0 * K;
+        A.w = w + (size_t)t0 * K;
+        A.L = L;
+        A.a = b.a;
+        A.gs = b.gs;
+        A.us = b.us;
+        A.zg = b.zg;
+        A.zu = b.zu;
+        A.hpre = b.hpre;
+        A.zres = b.zres;
+        A.y = y + (size_t)t0 * H;
+        A.st = st;
+        const int R = (H / GROUP) >= 32 ? 1 : 32 / (H / GROUP);
+        long warps = (long)Tc * (K + 1) * ((I + R - 1) / R) + 2 * rank;
+        const GateUpSmem gsm(Tc, H, K);
+        k_gateup<<<phase_grid(warps), PHASE_THREADS, gsm.total, s>>>(A);
+        if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+        const int RI = (I / GROUP) >= 32 ? 1 : 32 / (I / GROUP);
+        warps = (long)Tc * ((H + RI - 1) / RI);
+        const DownSmem dsm(Tc, I, K, sh != nullptr, rank, 0);
+        k_down<<<phase_grid(warps), PHASE_THREADS, dsm.total, s>>>(A);
+        if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+    }
+    return E0_OK;
+}
+
+// ---- prerouter head
+
+size_t head_ws_bytes(int T, int H, int hidden, int E, int K) {
+    WsCarve c{nullptr, 0};
+    c.take<float>((size_t)T * hidden);
+    c.take<float>((size_t)T * E);
+    c.take<float>((size_t)T * E);
+    (void)H;
+    (void)K;
+    return c.off + 256;
+}
+
+int prerouter_forward(const float* h, int T, const int32_t* inds_cur, const int32_t* inds_prev,
+                      const e0_prerouter* head, const e0_route_params* rp, float* logits_out, int32_t* inds_next,
+                      float* w_next, void* ws, uint32_t* st, cudaStream_t s) {
+    num_sms();
+    const int H = head->H, E = head->E, K = rp->K, hidden = head->hidden;
+    WsCarve c{reinterpret_cast<char*>(ws), 0};
+    float* hpre = c.take<float>((size_t)T * hidden);
+    float* zres = c.take<float>((size_t)T * E);
+    float* zbuf = c.take<float>((size_t)T * E);
+    float* z = logits_out ? logits_out : zbuf;
+    LayerP L = to_layer(nullptr, nullptr, nullptr, head, 0);
+    for (int t0 = 0; t0 < T; t0 += 8) {
+        const int Tc = T - t0 < 8 ? T - t0 : 8;
+        DecodeArgs A;
+        memset(&A, 0, sizeof(A));
+        A.T = Tc;
+        A.H = H;
+        A.I = GROUP;
+        A.E = E;
+        A.K = K;
+        A.x = h + (size_t)t0 * H;
+        A.inds = inds_cur + (size_t)t0 * K;
+        A.inds_prev = inds_prev ? inds_prev + (size_t)t0 * K : nullptr;
+        A.L = L;
+        A.hpre = hpre + (size_t)t0 * hidden;
+        A.zres = zres + (size_t)t0 * E;
+        A.z = z + (size_t)t0 * E;
+        A.st = st;
+        const int R = (H / GROUP) >= 32 ? 1 : 32 / (H / GROUP);
+        long warps = (long)Tc * ((hidden + E + R - 1) / R);
+        const GateUpSmem gsm(Tc, H, K);
+        k_gateup<<<phase_grid(warps), PHASE_THREADS, gsm.total, s>>>(A);
+        if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+        const int Rh = (hidden / GROUP) >= 32 ? 1 : 32 / (hidden / GROUP);
+        warps = (long)Tc * ((E + Rh - 1) / Rh);
+        const DownSmem dsm(Tc, GROUP, 0, false, 0, hidden);
+        k_down<<<phase_grid(warps), PHASE_THREADS, dsm.total, s>>>(A);
+        if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+    }
+    e0_route_params hr = *rp;
+    hr.logit_bias = nullptr;
+    return route(z, T, E, &hr, inds_next, w_next, st, s);
+}
+
+// ---- stack
+
+size_t stack_ws_bytes(int L, int H, int I, int E, int K, int hidden) {
+    return stack_layout(nullptr, nullptr, L, H, I, E, K, hidden, E0_MAX_LORA_RANK);
+}
+
+// Host copies of every prepared stack header, keyed by workspace address, so
+// that a step needs no device read-back (and can be captured in a graph).
+static std::mutex g_stack_mu;
+static std::map<const void*, StackHdr> g_stacks;
+
+int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, const e0_route_params* rp, void* ws,
+                  cudaStream_t s) {
+    num_sms();
+    int hidden = 0, rank = 0;
+    for (int l = 0; l < L; ++l) {
+        if (layers[l].head && layers[l].head->hidden > hidden) hidden = layers[l].head->hidden;
+        if (layers[l].shared && layers[l].shared->A_gate && layers[l].shared->rank > rank) rank = layers[l].shared->rank;
+    }
+    StackHdr hdr;
+    memset(&hdr, 0, sizeof(hdr));
+    stack_layout(&hdr, reinterpret_cast<char*>(ws), L, H, I, E, rp->K, hidden, E0_MAX_LORA_RANK);
+    hdr.L = L;
+    hdr.H = H;
+    hdr.I = I;
+    hdr.E = E;
+    hdr.K = rp->K;
+    hdr.hidden = hidden;
+    hdr.rank = rank;
+    hdr.rp = to_route(rp);
+    hdr.t = 0;
+    // persistent kernel geometry
+    const size_t gs = GateUpSmem(1, H, rp->K).total;
+    const size_t ds = DownSmem(1, I, rp->K, true, E0_MAX_LORA_RANK, hidden > 0 ? hidden : GROUP).total;
+    const size_t ps = gs > ds ? gs : ds;
+    const PersistSmem lay(H, E, rp->K, ps);
+    hdr.smem = (int32_t)ps;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_stack_token, PHASE_THREADS, lay.total);
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 2) per_sm = 2;
+    hdr.grid = num_sms() * per_sm;
+    LayerP* hl = new LayerP[L];
+    for (int l = 0; l < L; ++l)
+        hl[l] = to_layer(&layers[l].pool, layers[l].W_router, layers[l].shared, layers[l].head, layers[l].consumer);
+    int rc = E0_OK;
+    if (cudaMemcpyAsync(ws, &hdr, sizeof(hdr), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(hdr.layers, hl, sizeof(LayerP) * L, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemsetAsync(hdr.hist, 0xff, sizeof(int32_t) * 2 * L * rp->K, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        rc = E0_ERR_CUDA;
+    delete[] hl;
+    if (rc == E0_OK) {
+        std::lock_guard<std::mutex> g(g_stack_mu);
+        g_stacks[ws] = hdr;
+    }
+    return rc;
+}
+
+bool stack_known(const void* ws) {
+    std::lock_guard<std::mutex> g(g_stack_mu);
+    return g_stacks.count(ws) != 0;
+}
+
+int stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* trace, int impl, uint32_t* st,
+               cudaStream_t s) {
+    num_sms();
+    StackHdr* Sp = reinterpret_cast<StackHdr*>(ws);
+    StackHdr hdr;
+    {
+        std::lock_guard<std::mutex> g(g_stack_mu);
+        auto it = g_stacks.find(ws);
+        if (it == g_stacks.end()) return E0_ERR_ARG;
+        hdr = it->second;
+    }
+    TraceP tr;
+    memset(&tr, 0, sizeof(tr));
+    if (trace) {
+        tr.r = trace->r;
+        tr.inds = trace->inds;
+        tr.w = trace->w;
+        tr.head_logits = trace->head_logits;
+        tr.pred_inds = trace->pred_inds;
+    }
+    if (impl == 0) {
+        const PersistSmem lay(hdr.H, hdr.E, hdr.K, (size_t)hdr.smem);
+        void* args[] = {&Sp, (void*)&x, &r_out, &tr, &st};
+        return cuda_ok(cudaLaunchCooperativeKernel((const void*)k_stack_token, dim3(hdr.grid), dim3(PHASE_THREADS),
+                                                   args, lay.total, s));
+    }
+    const int H = hdr.H, I = hdr.I, E = hdr.E, K = hdr.K;
+    const int R = (H / GROUP) >= 32 ? 1 : 32 / (H / GROUP);
+    const size_t gsm = GateUpSmem(1, H, K).total;
+    const size_t dsm = DownSmem(1, I, K, true, E0_MAX_LORA_RANK, hdr.hidden > 0 ? hdr.hidden : GROUP).total;
+    const int RI = (I / GROUP) >= 32 ? 1 : 32 / (I / GROUP);
+    for (int l = 0; l < hdr.L; ++l) {
+        k_stack_norm<<<1, 256, 0, s>>>(Sp, l, x, tr);
+        k_stack_router<<<phase_grid((long)E / R + 1), PHASE_THREADS, 0, s>>>(Sp, l, st);
+        k_stack_resolve<<<1, 32, (size_t)E * 4, s>>>(Sp, l, tr, st);
+        k_stack_gateup<<<phase_grid((long)(K + 1) * I / R + 2 * hdr.rank + (hdr.hidden + E) / R), PHASE_THREADS,
+                         gsm, s>>>(Sp, l, st);
+        k_stack_down<<<phase_grid((long)H / RI + E), PHASE_THREADS, dsm, s>>>(Sp, l, x, r_out, st);
+        k_stack_head<<<1, 32, (size_t)E * 4, s>>>(Sp, l, tr, st);
+        if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+    }
+    k_stack_finish<<<1, 256, 0, s>>>(Sp, r_out, tr);
+    return launch_ok();
+}
+
+}  // namespace e0

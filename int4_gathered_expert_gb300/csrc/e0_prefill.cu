@@ -1,0 +1,707 @@
+// Whole-layer prefill ([PTKR] "SSD 전문가 스트리밍": the full-layer path loads a
+// layer's 9 tensors and computes with a sorted gather; [JAEHUN] "작동 원리":
+// prefill routes natively and never predicts):
+//   1. router logits on the tensor cores (fp16 X, fp16 W_r, fp32 accumulate);
+//   2. routing per token; tokens whose top-(K+1) logits are closer than
+//      REFINE_GAP get their logits recomputed with fp32 SIMT dot products
+//      before routing, so near-ties are decided as accurately as in decode;
+//   3. stable counting sort of the T*K assignments by expert;
+//   4. gather of the X rows into expert order;
+//   5. grouped GEMM gate/up on tcgen05 (int4 weights dequantised on chip into
+//      the 128-row M operand, tokens as the N operand), SwiGLU epilogue -> fp16;
+//   6. grouped GEMM down, epilogue scales by the routing weight -> fp32 rows;
+//   7. combine: Y[t] = sum over k (fixed order) of the token's K rows.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "e0_decode.cuh"
+#include "e0_internal.h"
+#include "e0_umma.cuh"
+
+namespace e0 {
+
+constexpr int SEG = 256;            // assignments per sort segment (one block)
+constexpr int BM = 128, BK = 64, BN = 128;
+constexpr int GEMM_THREADS = 192;   // warps 0-3 dequant + epilogue, 4 TMA, 5 MMA
+constexpr int STAGES = 4;
+constexpr float REFINE_GAP = 1e-3f;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+enum { MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
+
+struct PrefillWs {
+    float* logits;      // [T][E]
+    int32_t* inds;      // [T][K]
+    float* w;           // [T][K]
+    int32_t* counts;    // [E]
+    int32_t* offsets;   // [E+1]
+    int32_t* perm;      // [T*K]  sorted position -> assignment
+    int32_t* pos;       // [T*K]  assignment -> sorted position
+    int32_t* seg_cnt;   // [nseg][E]
+    int32_t* seg_base;  // [nseg][E]
+    int4* tiles;        // [max_tiles] {expert, first sorted row, n0, rows}
+    int32_t* flag;      // [T] tokens whose routing is recomputed in fp32
+    int32_t* n_tiles;   // [1]
+    uint32_t* err;      // [1] timeouts inside the GEMMs
+    float* wp;          // [T*K] routing weight per sorted row
+    __half* xp;         // [T*K][H] gathered rows
+    __half* abuf;       // [T*K][I] SwiGLU activations
+    float* yp;          // [T*K][H] weighted expert outputs
+    size_t bytes;
+    int max_tiles;
+};
+
+static PrefillWs prefill_ws(char* base, int T, int H, int I, int E, int K) {
+    const size_t A = (size_t)T * K;
+    const size_t nseg = (A + SEG - 1) / SEG;
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        off = (off + 1023) & ~(size_t)1023;
+        char* p = base + off;
+        off += n;
+        return p;
+    };
+    PrefillWs w;
+    w.max_tiles = (int)((A + BN - 1) / BN) + E;
+    w.logits = reinterpret_cast<float*>(take((size_t)T * E * 4));
+    w.inds = reinterpret_cast<int32_t*>(take(A * 4));
+    w.w = reinterpret_cast<float*>(take(A * 4));
+    w.counts = reinterpret_cast<int32_t*>(take((size_t)E * 4));
+    w.offsets = reinterpret_cast<int32_t*>(take((size_t)(E + 1) * 4));
+    w.perm = reinterpret_cast<int32_t*>(take(A * 4));
+    w.pos = reinterpret_cast<int32_t*>(take(A * 4));
+    w.seg_cnt = reinterpret_cast<int32_t*>(take(nseg * E * 4));
+    w.seg_base = reinterpret_cast<int32_t*>(take(nseg * E * 4));
+    w.tiles = reinterpret_cast<int4*>(take((size_t)w.max_tiles * 16));
+    w.flag = reinterpret_cast<int32_t*>(take((size_t)T * 4));
+    w.n_tiles = reinterpret_cast<int32_t*>(take(16));
+    w.err = reinterpret_cast<uint32_t*>(take(16));
+    w.wp = reinterpret_cast<float*>(take(A * 4));
+    w.xp = reinterpret_cast<__half*>(take(A * H * 2));
+    w.abuf = reinterpret_cast<__half*>(take(A * I * 2));
+    w.yp = reinterpret_cast<float*>(take(A * H * 4));
+    w.bytes = off + 1024;
+    return w;
+}
+
+size_t prefill_ws_bytes(int T, int H, int I, int E, int K) { return prefill_ws(nullptr, T, H, I, E, K).bytes; }
+
+// ------------------------------------------------------------------ stable counting sort
+
+__global__ void k_sort_hist(const int32_t* inds, int A, int E, int32_t* seg_cnt) {
+    extern __shared__ int32_t cnt[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int a = blockIdx.x * SEG + threadIdx.x;
+    if (a < A) {
+        const int e = inds[a];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) seg_cnt[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// one block of 1024 threads: totals, exclusive scan over experts, per-segment bases
+__global__ void k_sort_scan(const int32_t* seg_cnt, int nseg, int E, int32_t* counts, int32_t* offsets,
+                            int32_t* seg_base) {
+    __shared__ int32_t warp_tot[32];
+    const int e = threadIdx.x;
+    int c = 0;
+    if (e < E)
+        for (int s = 0; s < nseg; ++s) c += seg_cnt[(size_t)s * E + e];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
+        }
+        warp_tot[lane] = v;
+    }
+    __syncthreads();
+    const int excl = incl - c + (warp > 0 ? warp_tot[warp - 1] : 0);
+    if (e < E) {
+        counts[e] = c;
+        offsets[e] = excl;
+        int base = excl;
+        for (int s = 0; s < nseg; ++s) {
+            seg_base[(size_t)s * E + e] = base;
+            base += seg_cnt[(size_t)s * E + e];
+        }
+    }
+    if (e == E - 1) offsets[E] = excl + c;
+}
+
+__global__ void k_sort_scatter(const int32_t* inds, int A, int E, const int32_t* seg_base, int32_t* perm,
+                               int32_t* pos) {
+    __shared__ int32_t ex[SEG];
+    const int a = blockIdx.x * SEG + threadIdx.x;
+    const int e = a < A ? inds[a] : -1;
+    ex[threadIdx.x] = e;
+    __syncthreads();
+    if (a >= A || e < 0 || e >= E) return;
+    int rank = 0;
+    for (int j = 0; j < (int)threadIdx.x; ++j) rank += ex[j] == e;
+    const int p = seg_base[(size_t)blockIdx.x * E + e] + rank;
+    perm[p] = a;
+    if (pos) pos[a] = p;
+}
+
+static int sort_into(const int32_t* inds, int T, int K, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                     int32_t* pos, const PrefillWs& w, cudaStream_t s) {
+    const int A = T * K;
+    const int nseg = (A + SEG - 1) / SEG;
+    if (A == 0) {
+        if (cudaMemsetAsync(counts, 0, (size_t)E * 4, s) != cudaSuccess) return E0_ERR_CUDA;
+        if (cudaMemsetAsync(offsets, 0, (size_t)(E + 1) * 4, s) != cudaSuccess) return E0_ERR_CUDA;
+        return E0_OK;
+    }
+    k_sort_hist<<<nseg, SEG, (size_t)E * 4, s>>>(inds, A, E, w.seg_cnt);
+    k_sort_scan<<<1, 1024, 0, s>>>(w.seg_cnt, nseg, E, counts, offsets, w.seg_base);
+    k_sort_scatter<<<nseg, SEG, 0, s>>>(inds, A, E, w.seg_base, perm, pos);
+    return cudaGetLastError() == cudaSuccess ? E0_OK : E0_ERR_CUDA;
+}
+
+int prefill_sort(const int32_t* inds, int T, int K, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                 void* ws, cudaStream_t s) {
+    const PrefillWs w = prefill_ws(reinterpret_cast<char*>(ws), T, 64, 64, E, K);
+    return sort_into(inds, T, K, E, counts, offsets, perm, nullptr, w, s);
+}
+
+// ------------------------------------------------------------------ tcgen05 GEMM
+
+struct GemmP {
+    int K;              // reduction length (elements)
+    int rows_out;       // rows of A that exist (E for the router, I for gate/up, H for down)
+    // router
+    int T;
+    float* logits;
+    int E;
+    // grouped
+    const uint8_t* pool;
+    const int32_t* table;
+    int n_slots;
+    size_t slot_bytes;
+    int H, I;
+    const int4* tiles;
+    const int32_t* n_tiles;
+    __half* abuf;
+    float* yp;
+    const float* wp;
+    uint32_t* err;
+    uint32_t* st;
+};
+
+// One CTA computes one 128-row x BN-column output tile.  Roles:
+//   warps 0-3  (grouped modes) each thread dequantises one weight row of the
+//              A tile per K step into shared memory; afterwards all four warps
+//              drain the accumulator from TMEM (thread t owns TMEM lane t);
+//   warp 4     issues the TMA loads of the B tile (and of A for the router);
+//   warp 5     allocates TMEM and, from one thread, issues tcgen05.mma.
+// Pipeline: STAGES shared-memory stages guarded by full/empty mbarriers; the
+// MMA thread frees a stage with tcgen05.commit.  Every wait is time-bounded:
+// on timeout the CTA raises *err, stops its loops, frees TMEM and returns.
+template <int MODE>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_umma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmP p) {
+    constexpr int NA = MODE == MODE_GATEUP ? 2 : 1;
+    constexpr uint32_t A_BYTES = BM * BK * 2;
+    constexpr uint32_t B_BYTES = BN * BK * 2;
+    constexpr uint32_t STAGE_BYTES = NA * A_BYTES + B_BYTES;
+    constexpr uint32_t TMEM_COLS = NA * BN;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BM;
+    int expert = -1, row0, ncount;
+    if (MODE == MODE_ROUTER) {
+        row0 = blockIdx.y * BN;
+        ncount = min(BN, p.T - row0);
+    } else {
+        if ((int)blockIdx.y >= *p.n_tiles) return;
+        const int4 tl = p.tiles[blockIdx.y];
+        expert = tl.x;
+        row0 = tl.y;
+        ncount = tl.w;
+    }
+    if (ncount <= 0) return;
+    const int n_mma = (ncount + 15) & ~15;
+    const int nk = p.K / BK;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* accum = empty + STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+    volatile uint32_t* abort = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], MODE == MODE_ROUTER ? 1 : BM + 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accum, 1);
+        *abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const uint8_t* ex = nullptr;
+    if (MODE != MODE_ROUTER) {
+        int slot = -1;
+        if (expert >= 0) slot = p.table[expert];
+        if (slot >= 0 && slot < p.n_slots) ex = p.pool + (size_t)slot * p.slot_bytes;
+        else if (threadIdx.x == 0) set_status(p.st, E0_ST_SLOT_MISS);
+    }
+
+    if (warp < 4) {
+        // ---------------- dequant producers (grouped modes)
+        if (MODE != MODE_ROUTER) {
+            const int r = threadIdx.x;
+            const int row = m0 + r;
+            const bool live = ex != nullptr && row < p.rows_out;
+            const SlotLayout sl{p.H, p.I};
+            const uint8_t* c_a;
+            const uint8_t* c_b = nullptr;
+            const uint8_t* sb_a;
+            const uint8_t* sb_b = nullptr;
+            if (MODE == MODE_GATEUP) {
+                const int GH = p.H / GROUP;
+                c_a = ex + (size_t)row * p.H;
+                c_b = c_a + p.H / 2;
+                sb_a = ex + sl.gu_sb() + (size_t)(2 * row) * GH * 4;
+                sb_b = sb_a + (size_t)GH * 4;
+            } else {
+                const int GI = p.I / GROUP;
+                c_a = ex + sl.down_codes() + (size_t)row * (p.I / 2);
+                sb_a = ex + sl.down_sb() + (size_t)row * GI * 4;
+            }
+            constexpr int D = 4;  // K steps of codes kept in flight per thread
+            uint4 ra0[D], ra1[D], rb0[D], rb1[D];
+            uint32_t sa[D], sbv[D];
+#pragma unroll
+            for (int d = 0; d < D; ++d) {
+                if (live && d < nk) {
+                    ra0[d] = ldg_stream(c_a + d * 32);
+                    ra1[d] = ldg_stream(c_a + d * 32 + 16);
+                    sa[d] = ldg_u32(sb_a + d * 4);
+                    if (MODE == MODE_GATEUP) {
+                        rb0[d] = ldg_stream(c_b + d * 32);
+                        rb1[d] = ldg_stream(c_b + d * 32 + 16);
+                        sbv[d] = ldg_u32(sb_b + d * 4);
+                    }
+                }
+            }
+            bool ok = true;
+            for (int kb = 0; kb < nk && ok; kb += D) {
+#pragma unroll
+                for (int d = 0; d < D; ++d) {
+                    const int kk = kb + d;
+                    if (kk >= nk || !ok) break;
+                    const int s = kk % STAGES;
+                    if (!mbar_wait(&empty[s], ((kk / STAGES) + 1) & 1, abort, WAIT_LIMIT_NS)) {
+                        ok = false;
+                        *abort = 1;
+                        atomicOr(p.err, 1u);
+                        break;
+                    }
+                    uint8_t* a0 = smem + s * STAGE_BYTES;
+                    if (live) {
+                        dequant64_to_tile(ra0[d], ra1[d], sa[d], a0, r);
+                        if (MODE == MODE_GATEUP) dequant64_to_tile(rb0[d], rb1[d], sbv[d], a0 + A_BYTES, r);
+                    } else {
+                        zero_row_of_tile(a0, r);
+                        if (MODE == MODE_GATEUP) zero_row_of_tile(a0 + A_BYTES, r);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&full[s]);
+                    const int kn = kk + D;
+                    if (live && kn < nk) {
+                        ra0[d] = ldg_stream(c_a + kn * 32);
+                        ra1[d] = ldg_stream(c_a + kn * 32 + 16);
+                        sa[d] = ldg_u32(sb_a + kn * 4);
+                        if (MODE == MODE_GATEUP) {
+                            rb0[d] = ldg_stream(c_b + kn * 32);
+                            rb1[d] = ldg_stream(c_b + kn * 32 + 16);
+                            sbv[d] = ldg_u32(sb_b + kn * 4);
+                        }
+                    }
+                }
+            }
+        }
+        // ---------------- epilogue: TMEM -> registers -> global
+        const bool have = mbar_wait(accum, 0, abort, WAIT_LIMIT_NS);
+        if (!have) {
+            *abort = 1;
+            atomicOr(p.err, 2u);
+        }
+        tc_fence_after();
+        const int r = warp * 32 + lane;
+        const int row = m0 + r;
+        const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+        for (int c0 = 0; c0 < n_mma && have; c0 += 16) {
+            float acc[16];
+            tmem_ld16(tbase + c0, acc);
+            if (MODE == MODE_GATEUP) {
+                float up[16];
+                tmem_ld16(tbase + BN + c0, up);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = c0 + j;
+                    if (col < ncount && row < p.rows_out)
+                        p.abuf[(size_t)(row0 + col) * p.I + row] = __float2half_rn(silu_f(acc[j]) * up[j]);
+                }
+            } else if (MODE == MODE_DOWN) {
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = c0 + j;
+                    if (col < ncount && row < p.rows_out)
+                        p.yp[(size_t)(row0 + col) * p.H + row] = p.wp[row0 + col] * acc[j];
+                }
+            } else {
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = c0 + j;
+                    if (col < ncount && row < p.rows_out) p.logits[(size_t)(row0 + col) * p.E + row] = acc[j];
+                }
+            }
+        }
+    } else if (warp == 4) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmB);
+            if (MODE == MODE_ROUTER) tma_prefetch_desc(&tmA);
+            for (int kk = 0; kk < nk; ++kk) {
+                const int s = kk % STAGES;
+                if (!mbar_wait(&empty[s], ((kk / STAGES) + 1) & 1, abort, WAIT_LIMIT_NS)) {
+                    *abort = 1;
+                    atomicOr(p.err, 4u);
+                    break;
+                }
+                uint8_t* st = smem + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], B_BYTES + (MODE == MODE_ROUTER ? A_BYTES : 0u));
+                tma_load_2d(&tmB, &full[s], st + NA * A_BYTES, kk * BK, row0);
+                if (MODE == MODE_ROUTER) tma_load_2d(&tmA, &full[s], st, kk * BK, m0);
+            }
+        }
+    } else {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(BM, n_mma);
+            bool ok = true;
+            for (int kk = 0; kk < nk; ++kk) {
+                const int s = kk % STAGES;
+                if (!mbar_wait(&full[s], (kk / STAGES) & 1, abort, WAIT_LIMIT_NS)) {
+                    *abort = 1;
+                    atomicOr(p.err, 8u);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
+                const uint32_t b_addr = a_addr + NA * A_BYTES;
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j) {
+                    const uint64_t bd = sdesc_k_sw128(b_addr + j * 32);
+                    umma_f16(tmem, sdesc_k_sw128(a_addr + j * 32), bd, idesc, (kk | j) != 0);
+                    if (MODE == MODE_GATEUP)
+                        umma_f16(tmem + BN, sdesc_k_sw128(a_addr + A_BYTES + j * 32), bd, idesc, (kk | j) != 0);
+                }
+                umma_commit(&empty[s]);
+            }
+            if (ok) umma_commit(accum);
+        }
+    }
+    // drain: make sure no TMA write or MMA read of this CTA's shared memory is
+    // still in flight before the CTA exits (bounded by the same limit)
+    if (threadIdx.x == 160 && *abort) {
+        for (int s = 0; s < STAGES; ++s) mbar_wait(&empty[s], 0, abort, 1000000ull);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+template <int MODE>
+static size_t gemm_smem() {
+    constexpr int NA = MODE == MODE_GATEUP ? 2 : 1;
+    return (size_t)STAGES * (NA * BM * BK * 2 + BN * BK * 2) + 1024 + 256;
+}
+
+// ------------------------------------------------------------------ small prefill kernels
+
+// Route one token per warp from the tensor-core logits; flag tokens whose
+// top-(K+1) logits (plus bias) have a gap below REFINE_GAP.
+__global__ void k_prefill_route(const float* logits, int T, int E, RouteP rp, int32_t* inds, float* w,
+                                int32_t* flag, uint32_t* st) {
+    extern __shared__ float scr[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (t >= T) return;
+    const float* lg = logits + (size_t)t * E;
+    route_warp(lg, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr + warp * E, st, lane);
+    // smallest gap among the K+1 largest (biased) logits
+    float prev = INFINITY, mingap = INFINITY;
+    uint32_t taken[32];
+    const int MAXM = (E + 31) / 32;
+    for (int m = 0; m < 32; ++m) taken[m] = 0;
+    for (int k = 0; k <= rp.K && k < E; ++k) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int m = 0; m < MAXM; ++m) {
+            const int e = lane + 32 * m;
+            if (e < E && !taken[m]) {
+                const float v = lg[e] + (rp.logit_bias ? rp.logit_bias[e] : 0.f);
+                if (bi == 0x7fffffff || v > bv) {
+                    bv = v;
+                    bi = e;
+                }
+            }
+        }
+        for (int o = 16; o; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (bi == 0x7fffffff) break;
+        if ((bi & 31) == lane) taken[bi >> 5] = 1;
+        if (k > 0) mingap = fminf(mingap, prev - bv);
+        prev = bv;
+    }
+    if (lane == 0) flag[t] = (rp.mode != E0_ROUTE_SOFTMAX_TOPK || mingap < REFINE_GAP) ? 1 : 0;
+}
+
+// For flagged tokens: recompute the E logits with fp32 SIMT dot products (one
+// block per token) and route again.
+__global__ void __launch_bounds__(256) k_prefill_refine(const __half* X, int H, const __half* W_r, int E, RouteP rp,
+                                                        const int32_t* flag, float* logits, int32_t* inds, float* w,
+                                                        uint32_t* st) {
+    const int t = blockIdx.x;
+    if (!flag[t]) return;
+    extern __shared__ float sm[];
+    float* xs = sm;       // H
+    float* lg = sm + H;   // E
+    float* scr = lg + E;  // E
+    for (int j = threadIdx.x; j < H; j += blockDim.x) xs[j] = __half2float(X[(size_t)t * H + j]);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const RowMap rm(H, lane);
+    for (int e0 = warp * rm.R; e0 < E; e0 += nw * rm.R) {
+        const int e = e0 + rm.r;
+        float acc = 0.f;
+        if (rm.active && e < E) acc = h64_dot(W_r + (size_t)e * H + GROUP * rm.g, xs + GROUP * rm.g);
+        acc = seg_sum(acc, rm.G, lane);
+        if (rm.active && rm.g == 0 && e < E) lg[e] = acc;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) logits[(size_t)t * E + e] = lg[e];
+    if (warp == 0) route_warp(lg, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr, st, lane);
+}
+
+// tiles of up to BN consecutive sorted rows of one expert: {e, first row, n0, rows}
+__global__ void k_prefill_tiles(const int32_t* counts, const int32_t* offsets, int E, int4* tiles,
+                                int32_t* n_tiles) {
+    __shared__ int32_t warp_tot[32];
+    const int e = threadIdx.x;
+    const int c = e < E ? counts[e] : 0;
+    const int nt = (c + BN - 1) / BN;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
+        }
+        warp_tot[lane] = v;
+    }
+    __syncthreads();
+    const int start = incl - nt + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int j = 0; j < nt; ++j) {
+        const int n0 = j * BN;
+        tiles[start + j] = make_int4(e, offsets[e] + n0, n0, min(BN, c - n0));
+    }
+    if (threadIdx.x == blockDim.x - 1) *n_tiles = incl + (warp > 0 ? warp_tot[warp - 1] : 0);
+}
+
+// xp[p] = X[token of perm[p]], wp[p] = w[perm[p]]
+__global__ void k_prefill_gather(const __half* X, int H, int K, const int32_t* perm, const float* w, int A,
+                                 __half* xp, float* wp) {
+    const int row = blockIdx.x;
+    if (row >= A) return;
+    const int a = perm[row];
+    const int t = a / K;
+    if (threadIdx.x == 0) wp[row] = w[a];
+    const uint4* src = reinterpret_cast<const uint4*>(X + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)row * H);
+    for (int c = threadIdx.x; c < H / 8; c += blockDim.x) dst[c] = src[c];
+}
+
+// Y[t] = sum_k yp[pos[t*K + k]]  (k = 0..K-1, fixed order)
+__global__ void k_prefill_combine(const float* yp, const int32_t* pos, int T, int K, int H, float* Y) {
+    const int t = blockIdx.x;
+    for (int j = threadIdx.x * 4; j < H; j += blockDim.x * 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < K; ++k) {
+            const float4 v = *reinterpret_cast<const float4*>(yp + (size_t)pos[t * K + k] * H + j);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        *reinterpret_cast<float4*>(Y + (size_t)t * H + j) = acc;
+    }
+}
+
+__global__ void k_err_to_status(const uint32_t* err, uint32_t* st) {
+    if (threadIdx.x == 0 && *err) set_status(st, E0_ST_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D fp16 row-major [rows][inner] tensor, box = 64 elements x box_rows, 128B swizzle
+static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static std::once_flag g_prefill_init;
+static void prefill_attrs() {
+    cudaFuncSetAttribute(k_umma<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)gemm_smem<MODE_ROUTER>());
+    cudaFuncSetAttribute(k_umma<MODE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)gemm_smem<MODE_GATEUP>());
+    cudaFuncSetAttribute(k_umma<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem<MODE_DOWN>());
+}
+
+int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, const uint16_t* W_ru,
+                        const e0_route_params* rpp, float* Y, int32_t* inds_out, float* w_out, void* ws,
+                        uint32_t* st, cudaStream_t s) {
+    std::call_once(g_prefill_init, prefill_attrs);
+    const int H = bank->H, I = bank->I, E = bank->E, K = rpp->K;
+    if (H % BM || I % BM) return E0_ERR_UNSUPPORTED;
+    const __half* X = reinterpret_cast<const __half*>(Xu);
+    const __half* W_r = reinterpret_cast<const __half*>(W_ru);
+    PrefillWs w = prefill_ws(reinterpret_cast<char*>(ws), T, H, I, E, K);
+    const int A = T * K;
+    RouteP rp;
+    rp.mode = rpp->mode;
+    rp.K = K;
+    rp.n_groups = rpp->n_groups > 0 ? rpp->n_groups : 1;
+    rp.topk_groups = rpp->topk_groups > 0 ? rpp->topk_groups : 1;
+    rp.scale = rpp->scale;
+    rp.logit_bias = rpp->logit_bias;
+    int32_t* inds = inds_out ? inds_out : w.inds;
+    float* wts = w_out ? w_out : w.w;
+    if (cudaMemsetAsync(w.err, 0, 4, s) != cudaSuccess) return E0_ERR_CUDA;
+
+    CUtensorMap mWr, mX, mXp, mA;
+    if (!make_map(&mWr, W_r, H, E, BM) || !make_map(&mX, X, H, T, BN) || !make_map(&mXp, w.xp, H, A, BN) ||
+        !make_map(&mA, w.abuf, I, A, BN))
+        return E0_ERR_CUDA;
+
+    GemmP gp;
+    memset(&gp, 0, sizeof(gp));
+    gp.T = T;
+    gp.E = E;
+    gp.H = H;
+    gp.I = I;
+    gp.logits = w.logits;
+    gp.pool = bank->data;
+    gp.table = bank->slot_table;
+    gp.n_slots = bank->n_slots;
+    gp.slot_bytes = slot_bytes(H, I);
+    gp.tiles = w.tiles;
+    gp.n_tiles = w.n_tiles;
+    gp.abuf = w.abuf;
+    gp.yp = w.yp;
+    gp.wp = w.wp;
+    gp.err = w.err;
+    gp.st = st;
+
+    // 1. router logits
+    gp.K = H;
+    gp.rows_out = E;
+    k_umma<MODE_ROUTER><<<dim3((E + BM - 1) / BM, (T + BN - 1) / BN), GEMM_THREADS, gemm_smem<MODE_ROUTER>(), s>>>(
+        mWr, mX, gp);
+    // 2. routing (+ refinement of near-ties)
+    int32_t* flag = w.flag;
+    k_prefill_route<<<(T + 7) / 8, 256, (size_t)8 * E * 4, s>>>(w.logits, T, E, rp, inds, wts, flag, st);
+    k_prefill_refine<<<T, 256, (size_t)(H + 2 * E) * 4, s>>>(X, H, W_r, E, rp, flag, w.logits, inds, wts, st);
+    if (cudaGetLastError() != cudaSuccess) return E0_ERR_CUDA;
+    // 3. sort
+    int rc = sort_into(inds, T, K, E, w.counts, w.offsets, w.perm, w.pos, w, s);
+    if (rc) return rc;
+    k_prefill_tiles<<<1, 1024, 0, s>>>(w.counts, w.offsets, E, w.tiles, w.n_tiles);
+    // 4. gather
+    k_prefill_gather<<<A, 128, 0, s>>>(X, H, K, w.perm, wts, A, w.xp, w.wp);
+    // 5. gate/up
+    gp.K = H;
+    gp.rows_out = I;
+    k_umma<MODE_GATEUP><<<dim3(I / BM, w.max_tiles), GEMM_THREADS, gemm_smem<MODE_GATEUP>(), s>>>(mWr, mXp, gp);
+    // 6. down
+    gp.K = I;
+    gp.rows_out = H;
+    k_umma<MODE_DOWN><<<dim3(H / BM, w.max_tiles), GEMM_THREADS, gemm_smem<MODE_DOWN>(), s>>>(mWr, mA, gp);
+    // 7. combine
+    k_prefill_combine<<<T, 256, 0, s>>>(w.yp, w.pos, T, K, H, Y);
+    // a GEMM that gave up waiting surfaces as E0_ST_TIMEOUT
+    k_err_to_status<<<1, 32, 0, s>>>(w.err, st);
+    if (cudaGetLastError() != cudaSuccess) return E0_ERR_CUDA;
+    return E0_OK;
+}
+
+}  // namespace e0

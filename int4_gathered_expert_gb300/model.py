@@ -1,0 +1,141 @@
+"""Device-resident weights for the C ABI: uploads the canonical tensors drawn
+by ``synth``, packs experts into slot pools with e0_pack_experts and keeps the
+ctypes descriptors (and the torch tensors they point into) alive.  PyTorch is
+used for device memory and streams only; all arithmetic runs in libe0moe.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Dict, List, Optional
+
+import numpy as np
+import torch
+
+from . import lib as L
+
+
+def _dev(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device, non_blocking=False)
+
+
+class DeviceQBank:
+    """A layer's canonical stacked bank on the device (gate/up/down x codes/scale/bias)."""
+
+    def __init__(self, bank_np: Dict[str, Dict[str, np.ndarray]], device="cuda"):
+        self.t = {p: {k: _dev(v, device) for k, v in bank_np[p].items()} for p in ("gate", "up", "down")}
+        self.E = self.t["gate"]["codes"].shape[0]
+
+    def expert_q(self, e: int) -> L.ExpertQ:
+        def q(p):
+            d = self.t[p]
+            return L.QTensor(d["codes"][e].data_ptr(), d["scale"][e].data_ptr(), d["bias"][e].data_ptr())
+        return L.ExpertQ(q("gate"), q("up"), q("down"))
+
+
+class SlotPoolDev:
+    """n_slots experts in the kernel layout, a slot table [E] and an occupant
+    table [n_slots] (all -1 until something is packed)."""
+
+    def __init__(self, H: int, I: int, E: int, n_slots: int, device="cuda"):
+        self.H, self.I, self.E, self.n_slots = H, I, E, n_slots
+        self.slot_bytes = L.e0_slot_bytes(H, I)
+        self.data = torch.empty(n_slots * self.slot_bytes, dtype=torch.uint8, device=device)
+        self.table = torch.full((E,), -1, dtype=torch.int32, device=device)
+        self.occupant = torch.full((n_slots,), -1, dtype=torch.int32, device=device)
+        self.desc = L.SlotPool(self.data.data_ptr(), self.table.data_ptr(), self.occupant.data_ptr(),
+                               n_slots, H, I, E)
+
+    def pack(self, qbank: DeviceQBank, experts: List[int], slots: List[int], set_table=True, stream=None):
+        src = [qbank.expert_q(e) for e in experts]
+        L.e0_pack_experts(src, self.desc, slots, experts if set_table else None, stream=stream)
+
+    @classmethod
+    def resident(cls, bank_np, H, I, device="cuda", stream=None) -> "SlotPoolDev":
+        """Every expert of a layer in slot e (identity table)."""
+        qb = DeviceQBank(bank_np, device)
+        pool = cls(H, I, qb.E, qb.E, device)
+        ids = list(range(qb.E))
+        pool.pack(qb, ids, ids, stream=stream)
+        del qb
+        return pool
+
+
+class SharedDev:
+    """Shared expert (one packed slot) plus its LoRA tensors."""
+
+    def __init__(self, shared_np: dict, H: int, I: int, device="cuda", with_lora=True):
+        qb = DeviceQBank({p: {k: v[None] for k, v in shared_np["q"][p].items()} for p in ("gate", "up", "down")},
+                         device)
+        self.pool = SlotPoolDev(H, I, 1, 1, device)
+        self.pool.pack(qb, [0], [0])
+        self.lora = None
+        null = None
+        if with_lora and shared_np.get("lora") is not None:
+            self.lora = {p: {k: _dev(v, device) for k, v in shared_np["lora"][p].items()}
+                         for p in ("gate", "up", "down")}
+            lo = self.lora
+            self.desc = L.SharedExpert(self.pool.data.data_ptr(),
+                                       lo["gate"]["A"].data_ptr(), lo["gate"]["B"].data_ptr(),
+                                       lo["up"]["A"].data_ptr(), lo["up"]["B"].data_ptr(),
+                                       lo["down"]["A"].data_ptr(), lo["down"]["B"].data_ptr(),
+                                       int(shared_np["rank"]), float(shared_np["alpha"]))
+        else:
+            self.desc = L.SharedExpert(self.pool.data.data_ptr(), null, null, null, null, null, null, 0, 0.0)
+
+
+class HeadDev:
+    def __init__(self, head_np: dict, H: int, E: int, device="cuda"):
+        self.t = {k: _dev(v, device) for k, v in head_np.items() if v is not None}
+        hidden = self.t["fc1"].shape[0]
+        g = lambda k: self.t[k].data_ptr() if k in self.t else None  # noqa: E731
+        self.desc = L.Prerouter(g("fc1"), g("b1"), g("fc2"), g("b2"), g("lres"), H, E, hidden)
+        self.hidden = hidden
+
+
+class StackDev:
+    """A whole decode stack on the device plus its workspace and optional trace."""
+
+    def __init__(self, model, device="cuda", trace=False, with_lora=True):
+        sh = model.shape
+        s = sh.layer
+        self.shape = sh
+        self.H, self.I, self.E, self.K = s.H, s.I, s.E, s.K
+        self.L = len(model.banks)
+        self.pools = [SlotPoolDev.resident(b, s.H, s.I, device) for b in model.banks]
+        self.routers = [_dev(w, device) for w in model.routers]
+        self.heads = {l: HeadDev(h, s.H, s.E, device) for l, h in model.heads.items()}
+        self.shared = [SharedDev(x, s.H, s.I, device, with_lora) if x is not None else None for x in model.shared]
+        hidden = max([h.hidden for h in self.heads.values()], default=0)
+        self._sh_descs = [C.pointer(x.desc) if x is not None else None for x in self.shared]
+        self._hd_descs = {l: C.pointer(h.desc) for l, h in self.heads.items()}
+        consumers = set(sh.consumers)
+        layers = []
+        for l in range(self.L):
+            layers.append(L.StackLayer(self.pools[l].desc, self.routers[l].data_ptr(),
+                                       self._sh_descs[l] if self._sh_descs[l] is not None else None,
+                                       self._hd_descs.get(l), 1 if (l in consumers and (l - 1) in self.heads) else 0))
+        self.layers = layers
+        self.rp = L.route_params(0 if s.route == "softmax_topk" else 1, s.K, s.n_groups, s.topk_groups,
+                                 s.route_scale)
+        self.ws_bytes = L.e0_stack_workspace_size(self.L, s.H, s.I, s.E, s.K, hidden)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.r_out = torch.empty(s.H, dtype=torch.float32, device=device)
+        self.trace = None
+        if trace:
+            self.tr = {"r": torch.zeros((self.L + 1, s.H), dtype=torch.float32, device=device),
+                       "inds": torch.full((self.L, s.K), -1, dtype=torch.int32, device=device),
+                       "w": torch.zeros((self.L, s.K), dtype=torch.float32, device=device),
+                       "head_logits": torch.zeros((self.L, s.E), dtype=torch.float32, device=device),
+                       "pred_inds": torch.full((self.L, s.K), -1, dtype=torch.int32, device=device)}
+            self.trace = L.StackTrace(*[self.tr[k].data_ptr() for k in ("r", "inds", "w", "head_logits",
+                                                                           "pred_inds")])
+        self.prepare()
+
+    def prepare(self, stream=None):
+        L.e0_stack_prepare(self.layers, self.H, self.I, self.E, self.rp, self.ws, self.ws_bytes, stream=stream)
+
+    def step(self, x: torch.Tensor, impl: int = 0, stream=None, out: Optional[torch.Tensor] = None):
+        out = self.r_out if out is None else out
+        L.e0_stack_step(x, out, self.ws, self.trace, impl, self.status, stream=stream)
+        return out

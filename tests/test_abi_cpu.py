@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/e0moe.h declares; host-side argument checks answer without a GPU.
+No compute call is made here (CPU only)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "e0moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(e0_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int4_gathered_expert_gb300 import build, lib as L
+    if not os.path.exists(L.LIB_PATH):
+        try:
+            build.nvcc()
+        except RuntimeError:
+            pytest.skip("nvcc unavailable and the library is not built")
+        build.build()
+    return L.load()
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for must in ["e0_moe_block_forward", "e0_route_softmax_topk", "e0_route_sigmoid_group", "e0_prerouter_forward",
+                 "e0_slot_update", "e0_moe_prefill_forward", "e0_stack_step", "e0_pack_experts"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from int4_gathered_expert_gb300 import lib as L
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), n
+    # the binding covers the same names
+    assert set(L.exported_symbols()) == set(names)
+
+
+def test_sizes_without_gpu(lib):
+    from int4_gathered_expert_gb300 import lib as L
+    assert L.e0_slot_bytes(2048, 512) == 1_769_472
+    assert L.e0_slot_bytes(1536, 384) == 995_328
+    assert L.e0_slot_bytes(100, 64) == 0
+    assert L.e0_workspace_size(0, 8, 2048, 512, 256, 4) > 0
+    assert L.e0_stack_workspace_size(40, 2048, 512, 256, 4, 512) > 0
+    assert L.e0_stack_workspace_size(0, 2048, 512, 256, 4, 512) == 0
+
+
+def test_host_validation_codes(lib):
+    from int4_gathered_expert_gb300 import lib as L
+    # K > E, unsupported E, bad groups: rejected before any launch
+    assert lib.e0_route_softmax_topk(None, 4, 8, 9, None, None, None, None) == L.E0_ERR_ARG
+    assert lib.e0_route_softmax_topk(None, 4, 4096, 4, None, None, None, None) == L.E0_ERR_UNSUPPORTED
+    assert lib.e0_route_softmax_topk(None, 0, 16, 4, None, None, None, None) == L.E0_OK
+    assert lib.e0_route_softmax_topk(None, 4, 16, 4, None, None, None, None) == L.E0_ERR_NULL
+    assert lib.e0_route_sigmoid_group(None, 4, 128, 7, 4, 8, 2.5, None, None, None, None) == L.E0_ERR_ARG
+    assert lib.e0_route_sigmoid_group(None, 4, 128, 8, 9, 8, 2.5, None, None, None, None) == L.E0_ERR_ARG
+    assert lib.e0_route_sigmoid_group(None, 4, 128, 8, 1, 32, 2.5, None, None, None, None) == L.E0_ERR_ARG
+    pool = L.SlotPool(None, None, None, 8, 2048, 512, 256)
+    rp = L.route_params(K=4)
+    assert L.e0_moe_block_forward(None, 1, pool, None, rp, None, None, None, None, None, None, None, 0,
+                                  raise_on_error=False, stream=0) == L.E0_ERR_NULL
+    pool = L.SlotPool(16, 16, 16, 8, 2000, 512, 256)
+    assert L.e0_moe_block_forward(None, 1, pool, None, rp, None, None, None, None, None, None, None, 0,
+                                  raise_on_error=False, stream=0) == L.E0_ERR_UNSUPPORTED
+    assert lib.e0_stack_step(None, None, None, None, 0, None, None) == L.E0_ERR_NULL
+    assert lib.e0_stack_step(C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), None, 0, None, None) == L.E0_ERR_ARG
+    assert lib.e0_status_string(L.E0_ERR_CUDA).decode().startswith("CUDA")

@@ -1,0 +1,126 @@
+"""GPU parity of the whole-layer prefill (router GEMM, routing, stable sort by
+expert, tcgen05 grouped GEMMs, combine) against the CPU oracle."""
+import numpy as np
+import pytest
+
+from int4_gathered_expert_gb300 import synth
+from oracle import e0_oracle as O
+from tests.parity import REL_L2, rel_l2, routing_matches
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int4_gathered_expert_gb300 import build, lib
+    import os
+    if not os.path.exists(lib.LIB_PATH):
+        build.build()
+    lib.load()
+    return lib
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("T,K,E", [(1, 4, 16), (37, 4, 16), (4096, 4, 256), (300, 8, 128), (5, 1, 1024)])
+def test_prefill_sort_is_exact(L, T, K, E):
+    g = np.random.default_rng(T + K + E)
+    inds = np.stack([g.choice(E, size=K, replace=False) for _ in range(T)]).astype(np.int32)
+    if T > 10:
+        inds[: T // 3, 0] = 3  # a crowded expert
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    ws_bytes = L.e0_workspace_size(2, T, 64, 64, E, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    L.e0_prefill_sort(dev(inds), T, K, E, counts, offsets, perm, ws, ws_bytes)
+    c, o, p = O.prefill_sort(inds, E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(perm.cpu().numpy(), p)
+
+
+def run_prefill(L, pool, X16, Wr, rp, T):
+    s_H = pool.H
+    ws_bytes = L.e0_workspace_size(2, T, pool.H, pool.I, pool.E, rp.K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    Y = torch.empty((T, s_H), dtype=torch.float32, device="cuda")
+    inds = torch.empty((T, rp.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, rp.K), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.e0_moe_prefill_forward(X16, T, pool.desc, Wr, rp, Y, inds, w, ws, ws_bytes, st)
+    return Y.cpu().numpy(), inds.cpu().numpy(), w.cpu().numpy(), L.e0_read_status(st)
+
+
+@pytest.mark.parametrize("T", [1, 8, 130, 513])
+def test_tiny_prefill(L, T):
+    from int4_gathered_expert_gb300.model import SlotPoolDev
+    d = synth.tiny_layer(0, T=T)
+    s = d["shape"]
+    pool = SlotPoolDev.resident(d["bank"], s.H, s.I)
+    X = d["x"].astype(np.float16)
+    Y, inds, w, st = run_prefill(L, pool, dev(X), dev(d["router"]), L.route_params(K=s.K), T)
+    assert st == 0
+    Yo, rt = O.prefill(X, d["bank"], d["router"], s)
+    ex, msgs = routing_matches(inds, w, rt)
+    assert not msgs, msgs[:4]
+    errs = [rel_l2(Y[t], Yo[t]) for t in range(T) if t not in ex]
+    assert max(errs) <= REL_L2, max(errs)
+
+
+def test_prefill_one_crowded_expert_set(L):
+    """Every token routed to the same 4 experts: each expert gets T rows, so
+    the grouped GEMM runs several full N tiles plus a ragged tail."""
+    from int4_gathered_expert_gb300.model import SlotPoolDev
+    T = 300
+    d = synth.tiny_layer(3, T=T)
+    s = d["shape"]
+    pool = SlotPoolDev.resident(d["bank"], s.H, s.I)
+    bias = np.zeros(s.E, np.float32)
+    bias[[2, 5, 9, 14]] = 40.0
+    X = d["x"].astype(np.float16)
+    rp = L.route_params(K=s.K, logit_bias=dev(bias))
+    Y, inds, w, st = run_prefill(L, pool, dev(X), dev(d["router"]), rp, T)
+    assert st == 0
+    assert set(np.unique(inds)) == {2, 5, 9, 14}
+    Yo, rt = O.prefill(X, d["bank"], d["router"], s, logit_bias=bias)
+    ex, msgs = routing_matches(inds, w, rt)
+    assert not msgs
+    assert max(rel_l2(Y[t], Yo[t]) for t in range(T)) <= REL_L2
+
+
+@pytest.fixture(scope="module")
+def prefill35(L):
+    from int4_gathered_expert_gb300.model import SlotPoolDev
+    d = synth.prefill35b(4, T=4096)
+    s = d["shape"]
+    d["pool"] = SlotPoolDev.resident(d["bank"], s.H, s.I)
+    return d
+
+
+def test_35b_prefill_full_size(L, prefill35):
+    d = prefill35
+    s = d["shape"]
+    T = d["X"].shape[0]
+    rp = L.route_params(K=s.K, logit_bias=dev(d["logit_bias"]))
+    Y, inds, w, st = run_prefill(L, d["pool"], dev(d["X"]), dev(d["router"]), rp, T)
+    assert st == 0
+    # routing of every token against the oracle (exact up to the tie rule)
+    logits = O.router_logits(d["router"], d["X"], d["logit_bias"])
+    rt = O.route_softmax_topk(logits, s.K)
+    ex, msgs = routing_matches(inds, w, rt)
+    assert not msgs, msgs[:4]
+    # expert load is Zipf-like (the workload's recipe)
+    counts = np.bincount(inds.ravel(), minlength=s.E)
+    assert counts.sum() == T * s.K and counts.max() > 20 * np.median(counts)
+    # outputs on a sample of tokens, including the first and the last
+    g = np.random.default_rng(0)
+    sample = sorted(set([0, T - 1] + g.choice(T, 22, replace=False).tolist()) - set(ex))
+    Yo = O.moe_block(d["X"][sample].astype(np.float64), O.BankExperts(d["bank"]), rt.inds[sample], rt.w[sample])
+    errs = [rel_l2(Y[t], Yo[i]) for i, t in enumerate(sample)]
+    assert max(errs) <= REL_L2, max(errs)

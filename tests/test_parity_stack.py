@@ -1,0 +1,129 @@
+"""Decode-stack parity (35B tier: 40 layers, heads owned by 6..38; 8B tier: 24
+layers, sigmoid-group routing, heads owned by 7..22) against the CPU oracle,
+teacher-forced layer by layer: the oracle recomputes every checked layer from
+the GPU's residual stream and the GPU's routing, after checking that routing
+itself (native router or the head prediction made one token earlier)."""
+import numpy as np
+import pytest
+
+from int4_gathered_expert_gb300 import synth
+from oracle import e0_oracle as O
+from tests.parity import REL_L2, rel_l2, routing_matches
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+N_TOK = 6
+CHECK = (0, 1, 2, 5)
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int4_gathered_expert_gb300 import build, lib
+    import os
+    if not os.path.exists(lib.LIB_PATH):
+        build.build()
+    lib.load()
+    return lib
+
+
+def run_stack(sd, m, n_tok, impl):
+    sd.prepare()
+    traces = []
+    for t in range(n_tok):
+        sd.step(torch.from_numpy(m.x[t]).cuda(), impl=impl)
+        traces.append({k: v.cpu().numpy().copy() for k, v in sd.tr.items()})
+    return traces
+
+
+def check_stack(m, traces, check, L_check=None):
+    shape = m.shape
+    ls = shape.layer
+    nL = len(m.banks)
+    worst = 0.0
+    n_exempt = 0
+    for t in check:
+        tr = traces[t]
+        prev = traces[t - 1] if t > 0 else None
+        for l in (range(nL) if L_check is None else L_check):
+            r_in = tr["r"][l].astype(np.float64)
+            h = O.rmsnorm(r_in)
+            inds = tr["inds"][l]
+            w = tr["w"][l]
+            consumer = t > 0 and l in shape.consumers and (l - 1) in m.heads
+            if consumer:
+                # prediction as routing: exactly what the owner predicted one token earlier
+                assert np.array_equal(inds, prev["pred_inds"][l]), (t, l)
+            else:
+                rt = O.route(O.router_logits(m.routers[l], h[None]), ls)
+                ex, msgs = routing_matches(inds[None], w[None], rt)
+                assert not msgs, (t, l, msgs)
+                n_exempt += len(ex)
+            y_gpu = tr["r"][l + 1].astype(np.float64) - r_in
+            sh = m.shared[l] if m.shared else None
+            y_or = O.moe_block(h[None], O.BankExperts(m.banks[l]), inds[None].astype(np.int64),
+                               w[None].astype(np.float64), sh)[0]
+            e = rel_l2(y_gpu, y_or)
+            worst = max(worst, e)
+            assert e <= REL_L2, (t, l, e)
+            if l in m.heads:
+                p_inds = prev["inds"][l] if prev is not None else None
+                z = O.prerouter(h, inds, p_inds, m.heads[l])
+                assert rel_l2(tr["head_logits"][l], z) < 1e-5, (t, l)
+                if l + 1 < nL:
+                    # the prediction's indices (its weights are checked when it is consumed)
+                    rt = O.route(z[None], ls)
+                    gi = tr["pred_inds"][l + 1]
+                    if rt.gap[0] >= 1e-6 and rt.group_gap[0] >= 1e-6:
+                        assert set(gi) == set(rt.inds[0]), (t, l, gi, rt.inds[0])
+                    else:
+                        n_exempt += 1
+    return worst, n_exempt
+
+
+@pytest.fixture(scope="module")
+def stack35(L):
+    from int4_gathered_expert_gb300.model import StackDev
+    m = synth.stack_model(synth.STACK35B, n_tokens=N_TOK)
+    sd = StackDev(m, trace=True)
+    yield m, sd
+    del sd
+    torch.cuda.empty_cache()
+
+
+def test_35b_stack_teacher_forced_persistent(L, stack35):
+    m, sd = stack35
+    traces = run_stack(sd, m, N_TOK, impl=0)
+    assert L.e0_read_status(sd.status) == 0
+    worst, _ = check_stack(m, traces, CHECK)
+    print("35B stack worst per-layer rel-L2", worst)
+
+
+def test_35b_stack_chain_equals_persistent(L, stack35):
+    m, sd = stack35
+    a = run_stack(sd, m, 3, impl=0)
+    b = run_stack(sd, m, 3, impl=1)
+    for t in range(3):
+        for k in ("r", "inds", "pred_inds"):
+            assert np.array_equal(a[t][k], b[t][k]), (t, k)
+    check_stack(m, b, (1, 2), L_check=range(0, 40, 7))
+
+
+@pytest.fixture(scope="module")
+def stack8(L):
+    from int4_gathered_expert_gb300.model import StackDev
+    m = synth.stack_model(synth.STACK8B, n_tokens=N_TOK)
+    sd = StackDev(m, trace=True)
+    yield m, sd
+    del sd
+    torch.cuda.empty_cache()
+
+
+def test_8b_stack_teacher_forced(L, stack8):
+    m, sd = stack8
+    traces = run_stack(sd, m, N_TOK, impl=0)
+    assert L.e0_read_status(sd.status) == 0
+    worst, _ = check_stack(m, traces, CHECK)
+    print("8B stack worst per-layer rel-L2", worst)
