@@ -229,7 +229,7 @@ int e0_moe_prefill_forward(const uint16_t* X, int T, const e0_slot_pool* bank, c
     if (T == 0) return E0_OK;
     if (!X || !W_router || !Y || !ws) return E0_ERR_NULL;
     if (ws_bytes < e0_workspace_size(2, T, bank->H, bank->I, bank->E, rp->K)) return E0_ERR_ARG;
-    if (((uintptr_t)ws & 1023) || ((uintptr_t)X & 15) || ((uintptr_t)W_router & 15)) return E0_ERR_ARG;
+    if (((uintptr_t)ws & 255) || ((uintptr_t)X & 15) || ((uintptr_t)W_router & 15)) return E0_ERR_ARG;
     return e0::moe_prefill_forward(X, T, bank, W_router, rp, Y, inds_out, w_out, ws, d_status, cs(stream));
 }
 

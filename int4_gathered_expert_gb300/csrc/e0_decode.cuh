@@ -310,7 +310,8 @@ E0_DEV void phase_gateup(const DecodeArgs& A, const int32_t* inds, int blk, int 
         for (int q = warp; q < T * GH; q += nw)
             quantize_group_warp(A.x + (size_t)(q / GH) * H + GROUP * (q % GH), planes + q * 8, xg + q, lane, A.st);
     if (have_pool)
-        for (int q = threadIdx.x; q < T * K; q += blockDim.x) slots[q] = resolve_slot(A.L, E, inds[q], nullptr);
+        for (int q = threadIdx.x; q < T * K; q += blockDim.x)
+            slots[q] = resolve_slot(A.L, E, inds[q], blk == 0 ? A.st : nullptr);
     __syncthreads();
 
     const RowMap rm(H, lane);

@@ -59,7 +59,7 @@ static PrefillWs prefill_ws(char* base, int T, int H, int I, int E, int K) {
     const size_t nseg = (A + SEG - 1) / SEG;
     size_t off = 0;
     auto take = [&](size_t n) {
-        off = (off + 1023) & ~(size_t)1023;
+        off = (off + 255) & ~(size_t)255;
         char* p = base + off;
         off += n;
         return p;
@@ -83,7 +83,7 @@ static PrefillWs prefill_ws(char* base, int T, int H, int I, int E, int K) {
     w.xp = reinterpret_cast<__half*>(take(A * H * 2));
     w.abuf = reinterpret_cast<__half*>(take(A * I * 2));
     w.yp = reinterpret_cast<float*>(take(A * H * 4));
-    w.bytes = off + 1024;
+    w.bytes = off + 256;
     return w;
 }
 

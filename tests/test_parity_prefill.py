@@ -84,7 +84,8 @@ def test_prefill_one_crowded_expert_set(L):
     bias = np.zeros(s.E, np.float32)
     bias[[2, 5, 9, 14]] = 40.0
     X = d["x"].astype(np.float16)
-    rp = L.route_params(K=s.K, logit_bias=dev(bias))
+    bias_d = dev(bias)  # the descriptor holds a raw pointer: keep the tensor alive
+    rp = L.route_params(K=s.K, logit_bias=bias_d)
     Y, inds, w, st = run_prefill(L, pool, dev(X), dev(d["router"]), rp, T)
     assert st == 0
     assert set(np.unique(inds)) == {2, 5, 9, 14}
@@ -107,7 +108,8 @@ def test_35b_prefill_full_size(L, prefill35):
     d = prefill35
     s = d["shape"]
     T = d["X"].shape[0]
-    rp = L.route_params(K=s.K, logit_bias=dev(d["logit_bias"]))
+    bias_d = dev(d["logit_bias"])
+    rp = L.route_params(K=s.K, logit_bias=bias_d)
     Y, inds, w, st = run_prefill(L, d["pool"], dev(d["X"]), dev(d["router"]), rp, T)
     assert st == 0
     # routing of every token against the oracle (exact up to the tie rule)
