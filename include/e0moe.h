@@ -226,6 +226,28 @@ int e0_moe_block_forward(const float* x, int T, const e0_slot_pool* pool,
                          float* y, int32_t* inds_out, float* w_out,
                          void* ws, size_t ws_bytes, uint32_t* d_status, e0_stream_t stream);
 
+/* Same computation as e0_moe_block_forward, for callers that cannot hand the
+ * library a workspace: a plugin inside a host framework that owns every device
+ * allocation, or a serving loop with a fixed memory plan that must not
+ * allocate once it runs.  There is no counterpart on the pages this library
+ * follows; it is a deployment convenience.  The scratch is a fixed device
+ * array of E0_NOALLOC_SCRATCH_BYTES inside the library (each GPU that loads
+ * the library holds it until the process exits); a call whose workspace need
+ * (e0_workspace_size(0, ...)) exceeds it returns E0_ERR_UNSUPPORTED and
+ * launches nothing.  The call allocates nothing.  The first call on a device
+ * looks up the array's device address with that device current; make that
+ * first call before any stream capture.  All calls share the one array and it
+ * keeps the previous call's contents (nothing in it needs to start at zero):
+ * calls whose work overlaps on the GPU (other streams, other threads) race on
+ * it, so serialise them. */
+#define E0_NOALLOC_SCRATCH_BYTES (1u << 20)
+int e0_moe_block_forward_noalloc(const float* x, int T, const e0_slot_pool* pool,
+                                 const uint16_t* W_router, const e0_route_params* rp,
+                                 const int32_t* inds_in, const float* w_in,
+                                 const e0_shared_expert* shared,
+                                 float* y, int32_t* inds_out, float* w_out,
+                                 uint32_t* d_status, e0_stream_t stream);
+
 /* Prerouter head for T tokens: z = fc2 gelu_erf(fc1 f + b1) + b2 + lres f with
  * f = [h ; onehot(inds_cur) ; onehot(inds_prev)] (inds_prev NULL = all zeros,
  * the first token), then rp's routing of z gives the next layer's routing for

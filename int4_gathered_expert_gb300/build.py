@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libe0moe.so")
-SOURCES = ["e0_decode.cu", "e0_prefill.cu", "e0_abi.cu"]
+SOURCES = ["e0_decode.cu", "e0_prefill.cu", "e0_abi.cu", "e0_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -85,6 +85,8 @@ def load() -> C.CDLL:
         "e0_rmsnorm": (C.c_int, [vp, C.c_int, C.c_int, C.c_float, vp, vp]),
         "e0_moe_block_forward": (C.c_int, [vp, C.c_int, P(SlotPool), vp, P(RouteParams), vp, vp,
                                            P(SharedExpert), vp, vp, vp, vp, sz, vp, vp]),
+        "e0_moe_block_forward_noalloc": (C.c_int, [vp, C.c_int, P(SlotPool), vp, P(RouteParams), vp, vp,
+                                                   P(SharedExpert), vp, vp, vp, vp, vp]),
         "e0_prerouter_forward": (C.c_int, [vp, C.c_int, vp, vp, P(Prerouter), P(RouteParams), vp, vp, vp,
                                            vp, sz, vp, vp]),
         "e0_stack_workspace_size": (sz, [C.c_int] * 6),
@@ -108,7 +110,8 @@ def load() -> C.CDLL:
 def exported_symbols():
     """Names of the C entry points this binding declares."""
     return ["e0_slot_bytes", "e0_workspace_size", "e0_pack_experts", "e0_slot_update", "e0_route_softmax_topk",
-            "e0_route_sigmoid_group", "e0_rmsnorm", "e0_moe_block_forward", "e0_prerouter_forward",
+            "e0_route_sigmoid_group", "e0_rmsnorm", "e0_moe_block_forward", "e0_moe_block_forward_noalloc",
+            "e0_prerouter_forward",
             "e0_stack_workspace_size", "e0_stack_prepare", "e0_stack_step", "e0_prefill_sort",
             "e0_moe_prefill_forward", "e0_read_status", "e0_status_string"]
 
@@ -201,6 +204,17 @@ def e0_moe_block_forward(x, T, pool: SlotPool, W_router, rp: RouteParams, inds_i
                                      ptr(w_in), sh, ptr(y), ptr(inds_out), ptr(w_out), ptr(ws), ws_bytes,
                                      ptr(status), stream_handle(stream))
     return _check("e0_moe_block_forward", rc, raise_on_error)
+
+
+def e0_moe_block_forward_noalloc(x, T, pool: SlotPool, W_router, rp: RouteParams, inds_in, w_in, shared, y,
+                                 inds_out, w_out, status=None, stream=None, raise_on_error=True):
+    """e0_moe_block_forward without a workspace: the library's fixed scratch
+    array is used instead (see the header for its size and sharing rules)."""
+    sh = C.byref(shared) if shared is not None else None
+    rc = load().e0_moe_block_forward_noalloc(ptr(x), T, C.byref(pool), ptr(W_router), C.byref(rp), ptr(inds_in),
+                                             ptr(w_in), sh, ptr(y), ptr(inds_out), ptr(w_out), ptr(status),
+                                             stream_handle(stream))
+    return _check("e0_moe_block_forward_noalloc", rc, raise_on_error)
 
 
 def e0_prerouter_forward(h, T, inds_cur, inds_prev, head: Prerouter, rp: RouteParams, logits_out, inds_next,
