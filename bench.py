@@ -46,7 +46,61 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the timed CPU-oracle baseline")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--kernel-impl", type=int, default=0, help="0 persistent kernel, 1 per-phase chain")
+    p.add_argument("--layers", type=int, default=40, help="fewer layers: a small case for profiling only")
+    p.add_argument("--no-prefill", action="store_true", help="skip the whole-layer prefill measurement")
+    p.add_argument("--prefill-only", action="store_true")
     return p.parse_args()
+
+
+# ---------------------------------------------------------------- prefill (T=4096 whole-layer)
+
+
+def run_prefill_bench(dev, reps: int = 5):
+    """Whole-layer prefill of the 35B-tier layer, T=4096, Zipf(1.1) expert
+    load; the L2 is flushed (a 256 MB write) before every timed call."""
+    import torch
+    from int4_gathered_expert_gb300 import lib as L
+    from int4_gathered_expert_gb300 import synth
+    from int4_gathered_expert_gb300.model import SlotPoolDev
+    d = synth.prefill35b(4, T=4096)
+    s = d["shape"]
+    T = d["X"].shape[0]
+    pool = SlotPoolDev.resident(d["bank"], s.H, s.I)
+    X = torch.from_numpy(d["X"]).to(dev)
+    Wr = torch.from_numpy(d["router"]).to(dev)
+    bias = torch.from_numpy(d["logit_bias"]).to(dev)
+    rp = L.route_params(K=s.K, logit_bias=bias)
+    ws_bytes = L.e0_workspace_size(2, T, s.H, s.I, s.E, s.K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    Y = torch.empty((T, s.H), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    for _ in range(3):
+        L.e0_moe_prefill_forward(X, T, pool.desc, Wr, rp, Y, None, None, ws, ws_bytes, st, stream=stream)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            L.e0_moe_prefill_forward(X, T, pool.desc, Wr, rp, Y, None, None, ws, ws_bytes, st, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / 1e3)
+    t = float(np.median(times))
+    flops = 2.0 * T * s.K * 3 * s.H * s.I
+    pk = peaks()
+    peak = pk["bf16_tflops"] if pk else 1900.0
+    return {"workload": "35B-tier whole-layer prefill, T=4096, K=4, Zipf(1.1) expert load",
+            "value": T / t, "unit": "tok/s", "ms": t * 1e3, "useful_tflops": flops / t / 1e12,
+            "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peak, "unit": "TFLOP/s",
+                         "frac": flops / t / 1e12 / peak, "traffic": None,
+                         "peak_source": "MEASURED_PEAKS.json bf16_tflops (measured, fp16 = bf16 rate)"
+                         if pk else "fallback"},
+            "l2": "flushed (256 MB write) before each timed call", "device_status": int(st.item())}
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -234,7 +288,14 @@ def run_gb300(args):
     from int4_gathered_expert_gb300 import synth
     from int4_gathered_expert_gb300.model import StackDev
 
+    if args.prefill_only:
+        print(json.dumps({"prefill": run_prefill_bench(dev)}), flush=True)
+        return 0
     shape = synth.STACK35B
+    if args.layers != shape.n_layers:
+        import dataclasses
+        shape = dataclasses.replace(shape, n_layers=args.layers,
+                                    owners=tuple(o for o in shape.owners if o + 1 < args.layers))
     tps = args.tokens_per_step
     n_tok = (args.warmup + args.steps) * tps
     model = synth.stack_model(shape, n_tokens=n_tok)
@@ -281,7 +342,7 @@ def run_gb300(args):
         dist.barrier()
 
     value = ws * n_timed / (el_ms / 1e3)
-    nb = bytes_per_token(shape, native_layers=7)
+    nb = bytes_per_token(shape, native_layers=sum(1 for l in range(shape.n_layers) if l not in shape.consumers))
     mean_launch_s = float(np.mean(launch_ms)) / 1e3
     pk = peaks()
     peak = pk["hbm_gbs"] if pk else 6800.0
@@ -328,6 +389,12 @@ def run_gb300(args):
                "sample": f"first {n_cpu} tokens of the same stream (token 0 routes all 40 layers natively) "
                          "through the 40-layer stack, float64 numpy oracle"}
 
+    prefill = None
+    if rank == 0 and not args.no_prefill:
+        del sd
+        torch.cuda.empty_cache()
+        prefill = run_prefill_bench(dev)
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
@@ -345,7 +412,7 @@ def run_gb300(args):
                              "frac": achieved / peak, "traffic": traffic,
                              "kernel": "k_stack_token", "launch_us": mean_launch_s * 1e6,
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback"},
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_timed * (1 if args.kernel_impl == 0 else 241),
+                "cpu_baseline": cpu, "e2e": e2e, "prefill": prefill, "gpu_launches": n_timed * (1 if args.kernel_impl == 0 else 241),
                 "clocks": clocks, "device_status": st}
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -299,8 +299,16 @@ int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
 /* Decode one token: r_0 = x; for each layer h = rmsnorm(r) (eps 1e-6);
  * route (prediction or native); r += MoE(h) + Shared(h); owners evaluate their
  * head and store the next token's routing for layer+1.  x fp32 [H] device,
- * r_out fp32 [H] device.  impl: 0 = one persistent cooperative kernel for the
- * whole token, 1 = a chain of per-phase kernels (same arithmetic). */
+ * r_out fp32 [H] device.  impl selects the kernels (same arithmetic):
+ *   0 = one persistent cooperative kernel per token, two or three grid
+ *       barriers per layer (deterministic);
+ *   1 = a chain of per-phase kernels (deterministic, equal to 0 bit for bit);
+ *   2 = one cooperative launch of 8-CTA thread-block clusters per token, one
+ *       grid barrier per layer: each cluster computes a slice of the layer's
+ *       experts end to end, exchanging activations through distributed
+ *       shared memory, and adds its partial outputs with atomic adds (the
+ *       summation order, and so the last bits, may vary between runs).
+ *       E0_ERR_UNSUPPORTED when no cluster configuration fits the device. */
 int e0_stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* trace,
                   int impl, uint32_t* d_status, e0_stream_t stream);
 

@@ -192,6 +192,14 @@ struct StackHdr {
     float* z;            // [E]
     int32_t grid;        // blocks of the persistent kernel
     int32_t smem;        // its dynamic shared memory
+    // one-barrier-per-layer cluster kernel
+    unsigned long long bar_ctr;   // monotonic arrival counter
+    unsigned long long bar_base;  // its value when the next launch starts
+    float* y_acc;        // [3][H] layer outputs accumulated with red.add
+    float* hpre2;        // [2][hidden] head fc1 outputs, by layer parity
+    float* zres2;        // [2][E] head linear-residual outputs
+    float* z2;           // [2][E] head logits
+    int32_t grid2, smem2, teams;
 };
 
 struct TraceP {
@@ -233,7 +241,15 @@ static size_t stack_layout(StackHdr* hdr, char* base, int L, int H, int I, int E
     float* hp = c.take<float>(hidden > 0 ? hidden : 1);
     float* zr = c.take<float>(E);
     float* z = c.take<float>(E);
+    float* yacc = c.take<float>((size_t)3 * H);
+    float* hp2 = c.take<float>((size_t)2 * (hidden > 0 ? hidden : 1));
+    float* zr2 = c.take<float>((size_t)2 * E);
+    float* z2 = c.take<float>((size_t)2 * E);
     if (hdr) {
+        hdr->y_acc = yacc;
+        hdr->hpre2 = hp2;
+        hdr->zres2 = zr2;
+        hdr->z2 = z2;
         hdr->layers = layers;
         hdr->hist = hist;
         hdr->wcur = wcur;
@@ -286,17 +302,19 @@ E0_DEV bool layer_native(const StackHdr& S, const LayerP& L, int t) { return t =
 
 // Route the head logits z of owner layer `l` into the prediction consumed by
 // layer l+1 at the next token (one warp).
-E0_DEV void stack_route_head(const StackHdr& S, int l, int t, float* scr, TraceP tr, uint32_t* st, int lane) {
+E0_DEV void stack_route_head(const StackHdr& S, int l, int t, float* scr, TraceP tr, uint32_t* st, int lane,
+                             const float* z = nullptr) {
     if (l + 1 >= S.L) return;
+    if (z == nullptr) z = S.z;
     const int np = (t + 1) & 1;
     int32_t* pi = S.pred_inds + ((size_t)np * S.L + (l + 1)) * S.K;
     float* pw = S.pred_w + ((size_t)np * S.L + (l + 1)) * S.K;
     RouteP rp = S.rp;
     rp.logit_bias = nullptr;
-    route_warp(S.z, S.E, rp, pi, pw, scr, st, lane);
+    route_warp(z, S.E, rp, pi, pw, scr, st, lane);
     __syncwarp();
     if (tr.head_logits)
-        for (int e = lane; e < S.E; e += 32) tr.head_logits[(size_t)l * S.E + e] = __ldcg(S.z + e);
+        for (int e = lane; e < S.E; e += 32) tr.head_logits[(size_t)l * S.E + e] = __ldcg(z + e);
     if (tr.pred_inds && lane < S.K) tr.pred_inds[(size_t)(l + 1) * S.K + lane] = pi[lane];
 }
 
@@ -519,6 +537,8 @@ __global__ void __launch_bounds__(PHASE_THREADS) k_stack_token(StackHdr* Sp, con
     }
 }
 
+#include "e0_stack2.cuh"
+
 // ================================================================== host side
 
 static int g_num_sms = 0;
@@ -534,6 +554,7 @@ static void init_attrs() {
     cudaFuncSetAttribute(k_stack_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     cudaFuncSetAttribute(k_stack_down, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     cudaFuncSetAttribute(k_stack_token, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    cudaFuncSetAttribute(k_stack_token2, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
 }
 
 int num_sms() {
@@ -853,6 +874,35 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
     if (per_sm < 1) per_sm = 1;
     if (per_sm > 2) per_sm = 2;
     hdr.grid = num_sms() * per_sm;
+    // cluster kernel geometry: as many 8-CTA teams as can be resident at once
+    {
+        const T2Smem t2(H, E, L, rp->K);
+        hdr.smem2 = (int32_t)t2.total;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3((num_sms() / TEAM) * TEAM);
+        cfg.blockDim = dim3(T2_THREADS);
+        cfg.dynamicSmemBytes = t2.total;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = TEAM;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int ncl = 0;
+        if (cudaOccupancyMaxActiveClusters(&ncl, (void*)k_stack_token2, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            ncl = 0;
+        }
+        int teams = num_sms() / TEAM;
+        if (ncl < teams) teams = ncl;
+        // every team must hold at most T2_MAX_UNITS half-groups of the layer
+        const int nu = (rp->K + 1) * (I / 32);
+        if (teams > 0 && (nu + teams - 1) / teams > T2_MAX_UNITS) teams = 0;
+        hdr.teams = teams;
+        hdr.grid2 = teams * TEAM;
+    }
     LayerP* hl = new LayerP[L];
     for (int l = 0; l < L; ++l)
         hl[l] = to_layer(&layers[l].pool, layers[l].W_router, layers[l].shared, layers[l].head, layers[l].consumer);
@@ -860,6 +910,7 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
     if (cudaMemcpyAsync(ws, &hdr, sizeof(hdr), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(hdr.layers, hl, sizeof(LayerP) * L, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemsetAsync(hdr.hist, 0xff, sizeof(int32_t) * 2 * L * rp->K, s) != cudaSuccess ||
+        cudaMemsetAsync(hdr.y_acc, 0, sizeof(float) * 3 * H, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         rc = E0_ERR_CUDA;
     delete[] hl;
@@ -894,6 +945,32 @@ int stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* tra
         tr.w = trace->w;
         tr.head_logits = trace->head_logits;
         tr.pred_inds = trace->pred_inds;
+    }
+    if (impl == 2) {
+        if (hdr.teams < 1) return E0_ERR_UNSUPPORTED;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(hdr.grid2);
+        cfg.blockDim = dim3(T2_THREADS);
+        cfg.dynamicSmemBytes = (size_t)hdr.smem2;
+        cfg.stream = s;
+        cudaLaunchAttribute at[2];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = TEAM;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        at[1].id = cudaLaunchAttributeCooperative;
+        at[1].val.cooperative = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 2;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, k_stack_token2, Sp, x, r_out, tr, st);
+        if (e != cudaSuccess) {
+            // co-residency of a grid that fits on the device at once without the cooperative attribute
+            cudaGetLastError();
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, k_stack_token2, Sp, x, r_out, tr, st);
+        }
+        return cuda_ok(e);
     }
     if (impl == 0) {
         const PersistSmem lay(hdr.H, hdr.E, hdr.K, (size_t)hdr.smem);

@@ -27,7 +27,7 @@ constexpr int SEG = 256;            // assignments per sort segment (one block)
 constexpr int BM = 128, BK = 64, BN = 128;
 constexpr int GEMM_THREADS = 192;   // warps 0-3 dequant + epilogue, 4 TMA, 5 MMA
 constexpr int STAGES = 4;
-constexpr float REFINE_GAP = 1e-3f;
+constexpr float REFINE_GAP = 2e-4f;  // well above the error of fp32 tensor-core accumulation over K = H
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
 enum { MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
@@ -43,7 +43,7 @@ struct PrefillWs {
     int32_t* seg_cnt;   // [nseg][E]
     int32_t* seg_base;  // [nseg][E]
     int4* tiles;        // [max_tiles] {expert, first sorted row, n0, rows}
-    int32_t* flag;      // [T] tokens whose routing is recomputed in fp32
+    int32_t* flag;      // [T+1] tokens whose routing is recomputed in fp32 (count first)
     int32_t* n_tiles;   // [1]
     uint32_t* err;      // [1] timeouts inside the GEMMs
     float* wp;          // [T*K] routing weight per sorted row
@@ -76,7 +76,7 @@ static PrefillWs prefill_ws(char* base, int T, int H, int I, int E, int K) {
     w.seg_cnt = reinterpret_cast<int32_t*>(take(nseg * E * 4));
     w.seg_base = reinterpret_cast<int32_t*>(take(nseg * E * 4));
     w.tiles = reinterpret_cast<int4*>(take((size_t)w.max_tiles * 16));
-    w.flag = reinterpret_cast<int32_t*>(take((size_t)T * 4));
+    w.flag = reinterpret_cast<int32_t*>(take((size_t)(T + 1) * 4));
     w.n_tiles = reinterpret_cast<int32_t*>(take(16));
     w.err = reinterpret_cast<uint32_t*>(take(16));
     w.wp = reinterpret_cast<float*>(take(A * 4));
@@ -450,6 +450,240 @@ static size_t gemm_smem() {
     return (size_t)STAGES * (NA * BM * BK * 2 + BN * BK * 2) + 1024 + 256;
 }
 
+// ------------------------------------------------------------------ persistent grouped GEMM with TMA-fed dequant
+
+// One CTA per SM loops over work items (tile of up to P2_BN tokens of one
+// expert x one 128-row slice of its weights).  Roles:
+//   warps 0-3  dequantise: thread r turns row r of the raw int4 tile (loaded
+//              by TMA into shared memory) into fp16 in the 128B-swizzled
+//              K-major operand layout;
+//   warps 4-7  epilogue: drain one of two TMEM accumulators while the MMA
+//              fills the other;
+//   warp 8     TMA: raw code tile (3-D map over the slot pool) + token tile;
+//   warp 9     TMEM allocation and the tcgen05.mma issue.
+// In the gate/up GEMM a 128-row slice is 64 intermediate rows with the gate
+// and up rows interleaved (the slot layout stores them that way), so each
+// SwiGLU pair sits in adjacent TMEM lanes.
+constexpr int P2_STAGES = 5;
+constexpr int P2_THREADS = 320;
+constexpr int P2_BN = 128;
+constexpr uint32_t P2_A = 128 * 128;       // fp16 operand tile
+constexpr uint32_t P2_B = P2_BN * 128;     // token tile
+constexpr uint32_t P2_RAW = 128 * 32;      // raw int4 codes of one K step
+constexpr uint32_t P2_STAGE = P2_A + P2_B + P2_RAW;
+
+struct P2Item {
+    int slot, row0, ncount, m;
+};
+
+E0_DEV P2Item p2_item(const GemmP& p, int idx, int MT) {
+    const int4 tl = p.tiles[idx / MT];
+    P2Item it;
+    it.m = idx % MT;
+    it.row0 = tl.y;
+    it.ncount = tl.w;
+    const int s = (tl.x >= 0 && tl.x < p.E) ? p.table[tl.x] : -1;
+    it.slot = (s >= 0 && s < p.n_slots) ? s : -1;
+    return it;
+}
+
+E0_DEV void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(P2_THREADS, 1)
+    k_umma2(const __grid_constant__ CUtensorMap tmCodes, const __grid_constant__ CUtensorMap tmB, GemmP p) {
+    constexpr uint32_t TMEM_COLS = 2 * P2_BN;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int MT = MODE == MODE_GATEUP ? (2 * p.I) / 128 : p.H / 128;
+    const int n_items = *p.n_tiles * MT;
+    const int nk = p.K / BK;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + P2_STAGES * P2_STAGE);
+    uint64_t* a_full = raw_full + P2_STAGES;
+    uint64_t* empty = a_full + P2_STAGES;
+    uint64_t* acc_full = empty + P2_STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    volatile uint32_t* abort = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P2_STAGES; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&a_full[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(&acc_full[b2], 1);
+            mbar_init(&acc_empty[b2], 128);
+        }
+        *abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == 9) tmem_alloc(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const SlotLayout sl{p.H, p.I};
+
+    if (warp < 4) {
+        // ---------------- dequantisers
+        const int r = threadIdx.x;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            const P2Item it = p2_item(p, idx, MT);
+            const uint8_t* ex = it.slot >= 0 ? p.pool + (size_t)it.slot * p.slot_bytes : nullptr;
+            const int wr = it.m * 128 + r;  // weight row (interleaved gate/up rows for MODE_GATEUP)
+            const uint8_t* sbp = nullptr;
+            if (ex) {
+                if (MODE == MODE_GATEUP) sbp = ex + sl.gu_sb() + (size_t)wr * (p.H / GROUP) * 4;
+                else sbp = ex + sl.down_sb() + (size_t)wr * (p.I / GROUP) * 4;
+            }
+            for (int kk = 0; kk < nk; ++kk, ++g) {
+                const uint32_t s = g % P2_STAGES;
+                const uint32_t sbits = ex ? ldg_u32(sbp + kk * 4) : 0u;
+                if (!mbar_wait(&raw_full[s], (g / P2_STAGES) & 1, abort, WAIT_LIMIT_NS)) {
+                    ok = false;
+                    *abort = 1;
+                    atomicOr(p.err, 16u);
+                    break;
+                }
+                uint8_t* st = smem + s * P2_STAGE;
+                if (ex) {
+                    const uint4* rawp = reinterpret_cast<const uint4*>(st + P2_A + P2_B + r * 32);
+                    dequant64_to_tile(rawp[0], rawp[1], sbits, st, r);
+                } else {
+                    zero_row_of_tile(st, r);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&a_full[s]);
+            }
+        }
+    } else if (warp < 8) {
+        // ---------------- epilogue
+        const int q = threadIdx.x - 128;  // TMEM lane
+        const uint32_t tq = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        uint32_t ii = 0;
+        for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++ii) {
+            const P2Item it = p2_item(p, idx, MT);
+            const uint32_t buf = ii & 1;
+            const bool have = mbar_wait(&acc_full[buf], (ii >> 1) & 1, abort, WAIT_LIMIT_NS);
+            if (!have) {
+                *abort = 1;
+                atomicOr(p.err, 32u);
+            }
+            tc_fence_after();
+            const int n_mma = (it.ncount + 15) & ~15;
+            for (int c0 = 0; c0 < n_mma && have; c0 += 16) {
+                float acc[16];
+                tmem_ld16(tq + buf * P2_BN + c0, acc);
+                tmem_ld_wait();
+                if (MODE == MODE_GATEUP) {
+                    const int i = it.m * 64 + (q >> 1);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float other = __shfl_xor_sync(0xffffffffu, acc[j], 1);
+                        const int col = c0 + j;
+                        if (!(q & 1) && col < it.ncount)
+                            p.abuf[(size_t)(it.row0 + col) * p.I + i] = __float2half_rn(silu_f(acc[j]) * other);
+                    }
+                } else {
+                    const int jrow = it.m * 128 + q;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = c0 + j;
+                        if (col < it.ncount)
+                            p.yp[(size_t)(it.row0 + col) * p.H + jrow] = p.wp[it.row0 + col] * acc[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[buf]);
+        }
+    } else if (warp == 8) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmCodes);
+            tma_prefetch_desc(&tmB);
+            uint32_t g = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+                const P2Item it = p2_item(p, idx, MT);
+                const int z = it.slot >= 0 ? it.slot : 0;
+                for (int kk = 0; kk < nk; ++kk, ++g) {
+                    const uint32_t s = g % P2_STAGES;
+                    if (!mbar_wait(&empty[s], ((g / P2_STAGES) + 1) & 1, abort, WAIT_LIMIT_NS)) {
+                        ok = false;
+                        *abort = 1;
+                        atomicOr(p.err, 64u);
+                        break;
+                    }
+                    uint8_t* st = smem + s * P2_STAGE;
+                    mbar_arrive_expect_tx(&raw_full[s], P2_RAW + P2_B);
+                    tma_load_3d(&tmCodes, &raw_full[s], st + P2_A + P2_B, kk * 32, it.m * 128, z);
+                    tma_load_2d(&tmB, &raw_full[s], st + P2_A, kk * BK, it.row0);
+                }
+            }
+        }
+    } else {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            uint32_t g = 0, ii = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++ii) {
+                const P2Item it = p2_item(p, idx, MT);
+                const uint32_t buf = ii & 1;
+                if (!mbar_wait(&acc_empty[buf], ((ii >> 1) + 1) & 1, abort, WAIT_LIMIT_NS)) {
+                    *abort = 1;
+                    atomicOr(p.err, 128u);
+                    break;
+                }
+                tc_fence_after();
+                const int n_mma = (it.ncount + 15) & ~15;
+                const uint32_t idesc = idesc_f16_f32(128, n_mma);
+                for (int kk = 0; kk < nk; ++kk, ++g) {
+                    const uint32_t s = g % P2_STAGES;
+                    const uint32_t ph = (g / P2_STAGES) & 1;
+                    if (!mbar_wait(&raw_full[s], ph, abort, WAIT_LIMIT_NS) ||
+                        !mbar_wait(&a_full[s], ph, abort, WAIT_LIMIT_NS)) {
+                        ok = false;
+                        *abort = 1;
+                        atomicOr(p.err, 256u);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + s * P2_STAGE);
+                    const uint32_t b_addr = a_addr + P2_A;
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)
+                        umma_f16(tmem + buf * P2_BN, sdesc_k_sw128(a_addr + j * 32), sdesc_k_sw128(b_addr + j * 32),
+                                 idesc, (kk | j) != 0);
+                    umma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[buf]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+static size_t gemm2_smem() { return (size_t)P2_STAGES * P2_STAGE + 1024 + 256; }
+
 // ------------------------------------------------------------------ small prefill kernels
 
 // Route one token per warp from the tensor-core logits; flag tokens whose
@@ -493,34 +727,59 @@ __global__ void k_prefill_route(const float* logits, int T, int E, RouteP rp, in
         if (k > 0) mingap = fminf(mingap, prev - bv);
         prev = bv;
     }
-    if (lane == 0) flag[t] = (rp.mode != E0_ROUTE_SOFTMAX_TOPK || mingap < REFINE_GAP) ? 1 : 0;
+    if (lane == 0 && (rp.mode != E0_ROUTE_SOFTMAX_TOPK || mingap < REFINE_GAP)) flag[1 + atomicAdd(flag, 1)] = t;
 }
 
-// For flagged tokens: recompute the E logits with fp32 SIMT dot products (one
-// block per token) and route again.
-__global__ void __launch_bounds__(256) k_prefill_refine(const __half* X, int H, const __half* W_r, int E, RouteP rp,
-                                                        const int32_t* flag, float* logits, int32_t* inds, float* w,
-                                                        uint32_t* st) {
-    const int t = blockIdx.x;
-    if (!flag[t]) return;
-    extern __shared__ float sm[];
-    float* xs = sm;       // H
-    float* lg = sm + H;   // E
-    float* scr = lg + E;  // E
-    for (int j = threadIdx.x; j < H; j += blockDim.x) xs[j] = __half2float(X[(size_t)t * H + j]);
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const RowMap rm(H, lane);
-    for (int e0 = warp * rm.R; e0 < E; e0 += nw * rm.R) {
-        const int e = e0 + rm.r;
-        float acc = 0.f;
-        if (rm.active && e < E) acc = h64_dot(W_r + (size_t)e * H + GROUP * rm.g, xs + GROUP * rm.g);
-        acc = seg_sum(acc, rm.G, lane);
-        if (rm.active && rm.g == 0 && e < E) lg[e] = acc;
+// fp16 row slice (64 halves) . fp16 x slice (64 halves), fp32 accumulation
+E0_DEV float hh64_dot(const __half* wrow, const __half* x) {
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 wv = ldg_stream(wrow + 8 * c);
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + 8 * c);
+        const __half2* xh = reinterpret_cast<const __half2*>(&xv);
+        float xs[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(xh[i]);
+            xs[2 * i] = f.x;
+            xs[2 * i + 1] = f.y;
+        }
+        acc += h8_dot(wv, xs);
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) logits[(size_t)t * E + e] = lg[e];
-    if (warp == 0) route_warp(lg, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr, st, lane);
+    return acc;
+}
+
+// Exact (fp32 SIMT) logits of the flagged tokens: one warp per (token, row group).
+__global__ void __launch_bounds__(256) k_prefill_refine_logits(const __half* X, int H, const __half* W_r, int E,
+                                                               const int32_t* flag, float* logits) {
+    const int n = flag[0];
+    const int lane = threadIdx.x & 31;
+    const RowMap rm(H, lane);
+    const int per_tok = (E + rm.R - 1) / rm.R;
+    const long total = (long)n * per_tok;
+    for (long task = (long)blockIdx.x * 8 + (threadIdx.x >> 5); task < total; task += (long)gridDim.x * 8) {
+        const int t = flag[1 + task / per_tok];
+        const int e = (int)(task % per_tok) * rm.R + rm.r;
+        float acc = 0.f;
+        if (rm.active && e < E) acc = hh64_dot(W_r + (size_t)e * H + GROUP * rm.g, X + (size_t)t * H + GROUP * rm.g);
+        acc = seg_sum(acc, rm.G, lane);
+        if (rm.active && rm.g == 0 && e < E) logits[(size_t)t * E + e] = acc;
+    }
+}
+
+// Route the flagged tokens again from their exact logits (one warp each).
+__global__ void k_prefill_reroute(const float* logits, int E, RouteP rp, const int32_t* flag, int32_t* inds, float* w,
+                                  uint32_t* st) {
+    extern __shared__ float scr[];
+    const int n = flag[0];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = blockIdx.x * (blockDim.x >> 5) + warp; i < n; i += gridDim.x * (blockDim.x >> 5)) {
+        const int t = flag[1 + i];
+        route_warp(logits + (size_t)t * E, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr + warp * E, st,
+                   lane);
+        __syncwarp();
+    }
 }
 
 // tiles of up to BN consecutive sorted rows of one expert: {e, first row, n0, rows}
@@ -618,6 +877,21 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D uint8 [n_slots][rows][inner] view of one code region of every slot;
+// box = 32 bytes x 128 rows x 1 slot, no swizzle (dense 32-byte rows).
+static bool make_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t slots,
+                           uint64_t slot_stride) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {inner, rows, slots};
+    cuuint64_t strides[2] = {inner, slot_stride};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static std::once_flag g_prefill_init;
 static void prefill_attrs() {
     cudaFuncSetAttribute(k_umma<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -625,6 +899,8 @@ static void prefill_attrs() {
     cudaFuncSetAttribute(k_umma<MODE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)gemm_smem<MODE_GATEUP>());
     cudaFuncSetAttribute(k_umma<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem<MODE_DOWN>());
+    cudaFuncSetAttribute(k_umma2<MODE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm2_smem());
+    cudaFuncSetAttribute(k_umma2<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm2_smem());
 }
 
 int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, const uint16_t* W_ru,
@@ -679,8 +955,10 @@ int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, con
         mWr, mX, gp);
     // 2. routing (+ refinement of near-ties)
     int32_t* flag = w.flag;
+    if (cudaMemsetAsync(flag, 0, 4, s) != cudaSuccess) return E0_ERR_CUDA;
     k_prefill_route<<<(T + 7) / 8, 256, (size_t)8 * E * 4, s>>>(w.logits, T, E, rp, inds, wts, flag, st);
-    k_prefill_refine<<<T, 256, (size_t)(H + 2 * E) * 4, s>>>(X, H, W_r, E, rp, flag, w.logits, inds, wts, st);
+    k_prefill_refine_logits<<<num_sms() * 4, 256, 0, s>>>(X, H, W_r, E, flag, w.logits);
+    k_prefill_reroute<<<num_sms(), 256, (size_t)8 * E * 4, s>>>(w.logits, E, rp, flag, inds, wts, st);
     if (cudaGetLastError() != cudaSuccess) return E0_ERR_CUDA;
     // 3. sort
     int rc = sort_into(inds, T, K, E, w.counts, w.offsets, w.perm, w.pos, w, s);
@@ -688,14 +966,19 @@ int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, con
     k_prefill_tiles<<<1, 1024, 0, s>>>(w.counts, w.offsets, E, w.tiles, w.n_tiles);
     // 4. gather
     k_prefill_gather<<<A, 128, 0, s>>>(X, H, K, w.perm, wts, A, w.xp, w.wp);
-    // 5. gate/up
+    // 5. gate/up and 6. down: persistent grouped GEMMs, one CTA per SM
+    CUtensorMap mGU, mDN;
+    const size_t sbytes = slot_bytes(H, I);
+    if (!make_codes_map(&mGU, bank->data, (uint64_t)H / 2, (uint64_t)2 * I, (uint64_t)bank->n_slots, sbytes) ||
+        !make_codes_map(&mDN, bank->data + SlotLayout{H, I}.down_codes(), (uint64_t)I / 2, (uint64_t)H,
+                        (uint64_t)bank->n_slots, sbytes))
+        return E0_ERR_CUDA;
     gp.K = H;
-    gp.rows_out = I;
-    k_umma<MODE_GATEUP><<<dim3(I / BM, w.max_tiles), GEMM_THREADS, gemm_smem<MODE_GATEUP>(), s>>>(mWr, mXp, gp);
-    // 6. down
+    gp.rows_out = 2 * I;
+    k_umma2<MODE_GATEUP><<<num_sms(), P2_THREADS, gemm2_smem(), s>>>(mGU, mXp, gp);
     gp.K = I;
     gp.rows_out = H;
-    k_umma<MODE_DOWN><<<dim3(H / BM, w.max_tiles), GEMM_THREADS, gemm_smem<MODE_DOWN>(), s>>>(mWr, mA, gp);
+    k_umma2<MODE_DOWN><<<num_sms(), P2_THREADS, gemm2_smem(), s>>>(mDN, mA, gp);
     // 7. combine
     k_prefill_combine<<<T, 256, 0, s>>>(w.yp, w.pos, T, K, H, Y);
     // a GEMM that gave up waiting surfaces as E0_ST_TIMEOUT
