@@ -45,7 +45,8 @@ def parse():
     p.add_argument("--tokens-per-step", type=int, default=256)
     p.add_argument("--no-cpu", action="store_true", help="skip the timed CPU-oracle baseline")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--kernel-impl", type=int, default=0, help="0 persistent kernel, 1 per-phase chain")
+    p.add_argument("--kernel-impl", type=int, default=2,
+                   help="2 cluster kernel (default), 0 persistent cooperative kernel, 1 per-phase chain")
     p.add_argument("--layers", type=int, default=40, help="fewer layers: a small case for profiling only")
     p.add_argument("--no-prefill", action="store_true", help="skip the whole-layer prefill measurement")
     p.add_argument("--prefill-only", action="store_true")
@@ -219,6 +220,30 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (x itself without a process
+    group).  Works on any backend: the tensor lives on ``device`` (a CUDA
+    device for NCCL, the CPU for gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, seconds_max: float) -> float:
+    """Units processed by all ranks together over the slowest rank's time
+    (replicas: every rank does the same amount of work)."""
+    return world * units_per_rank / seconds_max
+
+
+# launches of this library's kernels per decode token, by stack implementation
+LAUNCHES_PER_TOKEN = {0: 1, 2: 1}
+KERNEL_NAME = {0: "k_stack_token", 1: "k_stack_gateup/k_stack_down chain", 2: "k_stack_token2"}
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 
 
@@ -335,19 +360,18 @@ def run_gb300(args):
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     st = int(sd.status.cpu().item())
     if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([el_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        el_ms = float(tt.item())
-        dist.barrier()
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    el_ms = max_over_ranks(el_ms, device=dev)
 
-    value = ws * n_timed / (el_ms / 1e3)
+    value = whole_job_rate(n_timed, ws, el_ms / 1e3)
     nb = bytes_per_token(shape, native_layers=sum(1 for l in range(shape.n_layers) if l not in shape.consumers))
     mean_launch_s = float(np.mean(launch_ms)) / 1e3
     pk = peaks()
     peak = pk["hbm_gbs"] if pk else 6800.0
     achieved = nb["total"] / mean_launch_s / 1e9
-    traffic = recorded_traffic("k_stack_token")
+    kname = KERNEL_NAME.get(args.kernel_impl, "?")
+    traffic = recorded_traffic(kname)
 
     # end to end: the same decode through the public API with host buffers
     e2e = None
@@ -374,16 +398,14 @@ def run_gb300(args):
             stream.synchronize()
         e2e_s = time.perf_counter() - w0
         if ws > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_s = float(tt.item())
-        e2e = {"value": ws * n_timed / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": tps * shape.layer.H * 4,
+            torch.distributed.barrier()
+        e2e_s = max_over_ranks(e2e_s, device=dev)
+        e2e = {"value": whole_job_rate(n_timed, ws, e2e_s), "unit": "tok/s", "h2d_bytes_per_step": tps * shape.layer.H * 4,
                "d2h_bytes_per_step": tps * shape.layer.H * 4}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        n_cpu = 2
+        n_cpu = 3
         el = time_oracle(model, n_cpu)
         cpu = {"value": n_cpu / el, "unit": "tok/s", "cores": cores(), "kind": "oracle",
                "sample": f"first {n_cpu} tokens of the same stream (token 0 routes all 40 layers natively) "
@@ -403,16 +425,17 @@ def run_gb300(args):
                 "config": {"workload": WORKLOAD, "tokens_per_step": tps, "batch": 1,
                            "l2": "no flush: each token streams %.0f MB of weights, more than the 129 MB L2"
                                  % (nb["total"] / 1e6),
-                           "kernel": "persistent cooperative kernel, one launch per token"
-                           if args.kernel_impl == 0 else "per-phase kernel chain"},
+                           "kernel": {0: "persistent cooperative kernel, one launch per token",
+                                      1: "per-phase kernel chain",
+                                      2: "cluster kernel (8-CTA teams), one launch per token"}.get(args.kernel_impl)},
                 "expert_weight_gbs": value * nb["routed"] / 1e9 / ws if ws else None,
                 "weight_gbs": value * nb["total"] / 1e9 / ws if ws else None,
                 "bytes_per_token": nb,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "traffic": traffic,
-                             "kernel": "k_stack_token", "launch_us": mean_launch_s * 1e6,
+                             "kernel": kname, "launch_us": mean_launch_s * 1e6,
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback"},
-                "cpu_baseline": cpu, "e2e": e2e, "prefill": prefill, "gpu_launches": n_timed * (1 if args.kernel_impl == 0 else 241),
+                "cpu_baseline": cpu, "e2e": e2e, "prefill": prefill, "gpu_launches": n_timed * LAUNCHES_PER_TOKEN.get(args.kernel_impl, 6 * shape.n_layers + 1),
                 "clocks": clocks, "device_status": st}
         print(json.dumps(line), flush=True)
     if ws > 1:

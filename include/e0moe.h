@@ -335,6 +335,21 @@ int e0_moe_prefill_forward(const uint16_t* X, int T, const e0_slot_pool* bank,
 
 /* ---- status ------------------------------------------------------------- */
 
+/* Largest wait e0_selftest_bounded_wait accepts, in microseconds. */
+#define E0_SELFTEST_MAX_WAIT_US 2000000u
+
+/* Exercise the device-side bounded wait that guards every spin in this
+ * library (grid barriers of the stack kernels, pipeline barriers of the
+ * prefill GEMMs): one thread polls *flag (caller-owned device word) until it
+ * is non-zero or limit_us microseconds of device time (globaltimer) have
+ * passed; on the time limit it ORs E0_ST_TIMEOUT into *d_status and returns.
+ * Nothing traps, so the context stays usable and a later e0_read_status
+ * reports the bit.  The pages describe no such call: it lets a caller (and the
+ * tests) check that a wait which never ends is turned into a status bit.
+ * Errors: NULL flag or d_status -> E0_ERR_NULL; limit_us == 0 or above
+ * E0_SELFTEST_MAX_WAIT_US -> E0_ERR_ARG. */
+int e0_selftest_bounded_wait(const uint32_t* flag, uint32_t limit_us, uint32_t* d_status, e0_stream_t stream);
+
 /* Copy *d_status to *h_out after everything queued on `stream`; synchronises
  * the stream. */
 int e0_read_status(const uint32_t* d_status, uint32_t* h_out, e0_stream_t stream);

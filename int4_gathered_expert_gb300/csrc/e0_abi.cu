@@ -233,6 +233,12 @@ int e0_moe_prefill_forward(const uint16_t* X, int T, const e0_slot_pool* bank, c
     return e0::moe_prefill_forward(X, T, bank, W_router, rp, Y, inds_out, w_out, ws, d_status, cs(stream));
 }
 
+int e0_selftest_bounded_wait(const uint32_t* flag, uint32_t limit_us, uint32_t* d_status, e0_stream_t stream) {
+    if (!flag || !d_status) return E0_ERR_NULL;
+    if (limit_us == 0 || limit_us > E0_SELFTEST_MAX_WAIT_US) return E0_ERR_ARG;
+    return e0::selftest_bounded_wait(flag, limit_us, d_status, cs(stream));
+}
+
 int e0_read_status(const uint32_t* d_status, uint32_t* h_out, e0_stream_t stream) {
     if (!d_status || !h_out) return E0_ERR_NULL;
     if (cudaMemcpyAsync(h_out, d_status, sizeof(uint32_t), cudaMemcpyDeviceToHost, cs(stream)) != cudaSuccess)

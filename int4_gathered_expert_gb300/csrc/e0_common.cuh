@@ -104,7 +104,8 @@ E0_DEV float2 ld2_shared_or_l2(const float* p) {
 E0_DEV int ldi_shared_or_l2(const int32_t* p) { return __isGlobal(p) ? __ldcg(p) : *p; }
 
 // One warp quantises group g of x (64 fp32 values) into planes + XGroup.
-E0_DEV void quantize_group_warp(const float* x, uint4* planes, XGroup* xg, int lane, uint32_t* st) {
+// Plane word k of the group is stored at planes[k * pstride].
+E0_DEV void quantize_group_warp(const float* x, uint4* planes, XGroup* xg, int lane, uint32_t* st, int pstride = 1) {
     const float2 v = ld2_shared_or_l2(x + 2 * lane);
     float mx = warp_max(fmaxf(fabsf(v.x), fabsf(v.y)));
     if (!(mx < 3.0e38f)) {  // NaN or inf in the activations
@@ -131,7 +132,7 @@ E0_DEV void quantize_group_warp(const float* x, uint4* planes, XGroup* xg, int l
         loA |= __shfl_xor_sync(0xffffffffu, loA, o);
         loB |= __shfl_xor_sync(0xffffffffu, loB, o);
     }
-    if ((lane & 3) == 0) planes[lane >> 2] = make_uint4(hiA, hiB, loA, loB);
+    if ((lane & 3) == 0) planes[(lane >> 2) * pstride] = make_uint4(hiA, hiB, loA, loB);
     if (lane == 0) {
         xg->c = mx / 32767.f;
         xg->sx = (float)s;
@@ -140,14 +141,14 @@ E0_DEV void quantize_group_warp(const float* x, uint4* planes, XGroup* xg, int l
 
 // Partial dot product of one 64-element group of an int4 row (two uint4 code
 // chunks = 8 words, kernel nibble order) with the matching activation planes;
-// sb = (scale, bias).
-E0_DEV float q4_group_dot(const uint4 c0, const uint4 c1, const uint4* pl, XGroup xg, uint32_t sb_bits) {
+// sb = (scale, bias).  Plane word k is read at pl[k * pstride].
+E0_DEV float q4_group_dot(const uint4 c0, const uint4 c1, const uint4* pl, XGroup xg, uint32_t sb_bits, int pstride = 1) {
     const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     int hi = 0;
     uint32_t lo = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint4 p = pl[k];
+        const uint4 p = pl[k * pstride];
         const uint32_t a = w[k] & 0x0F0F0F0Fu;
         const uint32_t b = (w[k] >> 4) & 0x0F0F0F0Fu;
         hi = dp4a_us(a, p.x, hi);

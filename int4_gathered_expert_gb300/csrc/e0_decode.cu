@@ -998,3 +998,34 @@ int stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* tra
 }
 
 }  // namespace e0
+
+// ================================================================== bounded-wait self-test
+
+namespace e0 {
+
+// One thread polls a flag the way every spin of this library does: bounded
+// by device time, ending in a status bit instead of a trap.
+__global__ void k_bounded_wait(const uint32_t* flag, uint64_t limit_ns, uint32_t* st) {
+    if (threadIdx.x != 0) return;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    while (true) {
+        uint32_t v;
+        asm volatile("ld.relaxed.gpu.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v) return;
+        uint64_t t1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+        if (t1 - t0 > limit_ns) {
+            set_status(st, E0_ST_TIMEOUT);
+            return;
+        }
+        __nanosleep(256);
+    }
+}
+
+int selftest_bounded_wait(const uint32_t* flag, uint32_t limit_us, uint32_t* st, cudaStream_t s) {
+    k_bounded_wait<<<1, 32, 0, s>>>(flag, (uint64_t)limit_us * 1000ull, st);
+    return cudaGetLastError() == cudaSuccess ? E0_OK : E0_ERR_CUDA;
+}
+
+}  // namespace e0

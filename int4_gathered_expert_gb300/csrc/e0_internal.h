@@ -9,6 +9,7 @@
 namespace e0 {
 
 int num_sms();
+int selftest_bounded_wait(const uint32_t* flag, uint32_t limit_us, uint32_t* st, cudaStream_t s);
 size_t slot_bytes(int H, int I);
 
 int pack_experts(const e0_expert_q* src, int n, const e0_slot_pool* dst, const int32_t* dst_slots,

@@ -165,6 +165,75 @@ E0_DEV float q4_half_dot(const uint4 c, const uint4* pl, XGroup xg, uint32_t sb_
     return xg.c * fmaf(__low2float(sb), (float)sqx, __high2float(sb) * xg.sx);
 }
 
+// ------------------------------------------------------------------ fp16 rows, one warp per row
+
+E0_DEV float h8_dot44(const uint4 wv, const float4 a, const float4 b) {
+    const __half2* hw = reinterpret_cast<const __half2*>(&wv);
+    const float2 w0 = __half22float2(hw[0]), w1 = __half22float2(hw[1]);
+    const float2 w2 = __half22float2(hw[2]), w3 = __half22float2(hw[3]);
+    float acc = w0.x * a.x;
+    acc = fmaf(w0.y, a.y, acc);
+    acc = fmaf(w1.x, a.z, acc);
+    acc = fmaf(w1.y, a.w, acc);
+    acc = fmaf(w2.x, b.x, acc);
+    acc = fmaf(w2.y, b.y, acc);
+    acc = fmaf(w3.x, b.z, acc);
+    return fmaf(w3.y, b.w, acc);
+}
+
+// This lane's part of an fp16 row (n halves, n a multiple of 8) times an fp32
+// vector in shared memory: the lane takes 8 consecutive elements out of every
+// 256, so one load of the warp covers 512 contiguous bytes of the row and the
+// shared-memory reads of neighbouring lanes do not collide.  Sum the lanes
+// with warp_sum.
+__device__ __noinline__ float hrow_dot(const __half* w, const float* x, int n, int lane) {
+    float acc = 0.f;
+    for (int c0 = 0; c0 < n; c0 += 4 * 256) {
+        uint4 wv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int c = c0 + k * 256 + lane * 8;
+            if (c < n) wv[k] = ldg_stream(w + c);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int c = c0 + k * 256 + lane * 8;
+            if (c < n)
+                acc += h8_dot44(wv[k], *reinterpret_cast<const float4*>(x + c), *reinterpret_cast<const float4*>(x + c + 4));
+        }
+    }
+    return acc;
+}
+
+// Same for the head's second layer: x = gelu_erf(hp), hp written by other
+// blocks earlier in the launch (read from L2).
+__device__ __noinline__ float hrow_dot_gelu(const __half* w, const float* hp, int n, int lane) {
+    float acc = 0.f;
+    for (int c0 = 0; c0 < n; c0 += 2 * 256) {
+        uint4 wv[2];
+        float4 a[2], b[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int c = c0 + k * 256 + lane * 8;
+            if (c < n) {
+                wv[k] = ldg_stream(w + c);
+                a[k] = __ldcg(reinterpret_cast<const float4*>(hp + c));
+                b[k] = __ldcg(reinterpret_cast<const float4*>(hp + c + 4));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int c = c0 + k * 256 + lane * 8;
+            if (c < n) {
+                const float4 ga = make_float4(gelu_erf_f(a[k].x), gelu_erf_f(a[k].y), gelu_erf_f(a[k].z), gelu_erf_f(a[k].w));
+                const float4 gb = make_float4(gelu_erf_f(b[k].x), gelu_erf_f(b[k].y), gelu_erf_f(b[k].z), gelu_erf_f(b[k].w));
+                acc += h8_dot44(wv[k], ga, gb);
+            }
+        }
+    }
+    return acc;
+}
+
 // ------------------------------------------------------------------ shared memory layout
 
 struct T2Smem {
@@ -339,14 +408,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 
         // ---- routing of native layers: logits on every warp of the grid, one grid barrier
         if (native) {
-            const RowMap rm(H, lane);
-            const int nrow = (E + rm.R - 1) / rm.R;
-            for (int task = b * NW + warp; task < nrow; task += nb * NW) {
-                const int e = task * rm.R + rm.r;
-                float acc = 0.f;
-                if (rm.active && e < E) acc = h64_dot(L.W_r + (size_t)e * H + GROUP * rm.g, h + GROUP * rm.g);
-                acc = seg_sum(acc, rm.G, lane);
-                if (rm.active && rm.g == 0 && e < E) S.logits[e] = acc;
+            for (int e = b * NW + warp; e < E; e += nb * NW) {
+                const float acc = warp_sum(hrow_dot(L.W_r + (size_t)e * H, h, H, lane));
+                if (lane == 0) S.logits[e] = acc;
             }
             grid_barrier2(Sp, bar0 + (unsigned long long)(++nbar) * nb, st);
             if (warp == 0) {
@@ -357,6 +421,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                     slot_s[lane] = (s2 >= 0 && s2 < L.n_slots) ? L.pool + (size_t)s2 * sbytes : nullptr;
                 }
             }
+            __syncthreads();  // warp 0's routing is read by every warp below
         }
         if (b == 0 && warp == 1 && lane < K) {
             const int e = inds_s[lane];
@@ -366,8 +431,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             if (tr.inds) tr.inds[(size_t)l * K + lane] = e;
             if (tr.w) tr.w[(size_t)l * K + lane] = w_s[lane];
         }
-        // planes of h
-        for (int g = warp; g < GH; g += NW) quantize_group_warp(h + GROUP * g, hpl + g * 8, hxg + g, lane, nullptr);
+        // planes of h: word k of group g sits at hpl[k * GH + g], so lanes that
+        // read consecutive groups touch consecutive 16-byte words
+        for (int g = warp; g < GH; g += NW) quantize_group_warp(h + GROUP * g, hpl + g, hxg + g, lane, nullptr, GH);
         __syncthreads();
 
         const T2Split sp(I, nk, team, NT);
@@ -428,8 +494,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                     const int pr = pb + v * step + rm.r;
                     float pg = 0.f, pu = 0.f;
                     if (exs[v]) {
-                        pg = q4_group_dot(c[v][0], c[v][1], hpl + rm.g * 8, hxg[rm.g], sbv[v][0]);
-                        pu = q4_group_dot(c[v][2], c[v][3], hpl + rm.g * 8, hxg[rm.g], sbv[v][1]);
+                        pg = q4_group_dot(c[v][0], c[v][1], hpl + rm.g, hxg[rm.g], sbv[v][0], GH);
+                        pu = q4_group_dot(c[v][2], c[v][3], hpl + rm.g, hxg[rm.g], sbv[v][1], GH);
                     }
                     pg = seg_sum(pg, rm.G, lane);
                     pu = seg_sum(pu, rm.G, lane);
@@ -540,60 +606,31 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                 stack_route_head(S, l - 2, t, scr, tr, st, lane, S.z2 + (size_t)((l - 1) & 1) * E);
             const LayerP P = l >= 1 ? S.layers[l - 1] : L;
             const int hidP = (l >= 1 && P.fc1) ? P.hidden : 0;
-            const RowMap r2(hidP > 0 ? hidP : GROUP, lane);
-            const int n_fc2 = hidP > 0 ? (E + r2.R - 1) / r2.R : 0;
-            const RowMap r1(H, lane);
-            const int n_fc1 = L.fc1 ? (L.hidden + r1.R - 1) / r1.R : 0;
-            const int n_lres = L.fc1 ? (E + r1.R - 1) / r1.R : 0;
+            const int n_fc2 = hidP > 0 ? E : 0;
+            const int n_fc1 = L.fc1 ? L.hidden : 0;
+            const int n_lres = L.fc1 ? E : 0;
             const int32_t* prev = t > 0 ? S.hist + ((size_t)((t + 1) & 1) * Lz + l) * K : nullptr;
             for (int it = aw; it < n_fc2 + n_fc1 + n_lres; it += naw) {
                 if (it < n_fc2) {
-                    const int e = it * r2.R + r2.r;
-                    float acc = 0.f;
-                    if (r2.active && e < E) {
-                        const float* hp = S.hpre2 + (size_t)((l - 1) & 1) * hidP + GROUP * r2.g;
-                        const __half* wr = P.fc2 + (size_t)e * hidP + GROUP * r2.g;
-                        uint4 wv[8];
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) wv[c] = ldg_stream(wr + 8 * c);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            float gx[8];
-                            const float4 a0 = __ldcg(reinterpret_cast<const float4*>(hp + 8 * c));
-                            const float4 a1 = __ldcg(reinterpret_cast<const float4*>(hp + 8 * c + 4));
-                            gx[0] = gelu_erf_f(a0.x);
-                            gx[1] = gelu_erf_f(a0.y);
-                            gx[2] = gelu_erf_f(a0.z);
-                            gx[3] = gelu_erf_f(a0.w);
-                            gx[4] = gelu_erf_f(a1.x);
-                            gx[5] = gelu_erf_f(a1.y);
-                            gx[6] = gelu_erf_f(a1.z);
-                            gx[7] = gelu_erf_f(a1.w);
-                            acc += h8_dot(wv[c], gx);
-                        }
-                    }
-                    acc = seg_sum(acc, r2.G, lane);
-                    if (r2.active && r2.g == 0 && e < E)
+                    const int e = it;
+                    const float acc = warp_sum(
+                        hrow_dot_gelu(P.fc2 + (size_t)e * hidP, S.hpre2 + (size_t)((l - 1) & 1) * hidP, hidP, lane));
+                    if (lane == 0)
                         S.z2[(size_t)(l & 1) * E + e] = acc + (P.b2 ? __half2float(P.b2[e]) : 0.f) +
                                                         __ldcg(S.zres2 + (size_t)((l - 1) & 1) * E + e);
                 } else {
                     const int q = it - n_fc2;
                     const bool is_fc1 = q < n_fc1;
-                    const int row = (is_fc1 ? q : q - n_fc1) * r1.R + r1.r;
-                    const int nrows = is_fc1 ? L.hidden : E;
-                    const __half* Wm = is_fc1 ? L.fc1 : L.lres;
-                    const size_t ld = (size_t)H + 2 * E;
-                    float acc = 0.f;
-                    if (r1.active && row < nrows) {
-                        const __half* wr = Wm + (size_t)row * ld;
-                        acc = h64_dot(wr + GROUP * r1.g, h + GROUP * r1.g);
-                        for (int c = r1.g; c < 2 * K; c += r1.G) {
-                            const int e = c < K ? inds_s[c] : (prev ? __ldcg(prev + c - K) : -1);
-                            if (e >= 0 && e < E) acc += __half2float(wr[(c < K ? (size_t)H : (size_t)H + E) + e]);
-                        }
+                    const int row = is_fc1 ? q : q - n_fc1;
+                    const __half* wr = (is_fc1 ? L.fc1 : L.lres) + (size_t)row * ((size_t)H + 2 * E);
+                    float acc = hrow_dot(wr, h, H, lane);
+                    // the one-hot columns: this layer's experts, then the previous token's
+                    if (lane < 2 * K) {
+                        const int e = lane < K ? inds_s[lane] : (prev ? __ldcg(prev + lane - K) : -1);
+                        if (e >= 0 && e < E) acc += __half2float(wr[(lane < K ? (size_t)H : (size_t)H + E) + e]);
                     }
-                    acc = seg_sum(acc, r1.G, lane);
-                    if (r1.active && r1.g == 0 && row < nrows) {
+                    acc = warp_sum(acc);
+                    if (lane == 0) {
                         if (is_fc1)
                             S.hpre2[(size_t)(l & 1) * L.hidden + row] = acc + (L.b1 ? __half2float(L.b1[row]) : 0.f);
                         else

@@ -96,6 +96,7 @@ def load() -> C.CDLL:
         "e0_prefill_sort": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, vp, vp, vp, vp, sz, vp]),
         "e0_moe_prefill_forward": (C.c_int, [vp, C.c_int, P(SlotPool), vp, P(RouteParams), vp, vp, vp,
                                              vp, sz, vp, vp]),
+        "e0_selftest_bounded_wait": (C.c_int, [vp, C.c_uint32, vp, vp]),
         "e0_read_status": (C.c_int, [vp, P(C.c_uint32), vp]),
         "e0_status_string": (C.c_char_p, [C.c_int]),
     }
@@ -113,7 +114,7 @@ def exported_symbols():
             "e0_route_sigmoid_group", "e0_rmsnorm", "e0_moe_block_forward", "e0_moe_block_forward_noalloc",
             "e0_prerouter_forward",
             "e0_stack_workspace_size", "e0_stack_prepare", "e0_stack_step", "e0_prefill_sort",
-            "e0_moe_prefill_forward", "e0_read_status", "e0_status_string"]
+            "e0_moe_prefill_forward", "e0_selftest_bounded_wait", "e0_read_status", "e0_status_string"]
 
 
 # ---------------------------------------------------------------- marshalling
@@ -254,6 +255,14 @@ def e0_moe_prefill_forward(X, T, bank: SlotPool, W_router, rp: RouteParams, Y, i
                                        ptr(inds_out), ptr(w_out), ptr(ws), ws_bytes, ptr(status),
                                        stream_handle(stream))
     return _check("e0_moe_prefill_forward", rc, raise_on_error)
+
+
+E0_SELFTEST_MAX_WAIT_US = 2000000
+
+
+def e0_selftest_bounded_wait(flag, limit_us, status, stream=None, raise_on_error=True):
+    rc = load().e0_selftest_bounded_wait(ptr(flag), int(limit_us), ptr(status), stream_handle(stream))
+    return _check("e0_selftest_bounded_wait", rc, raise_on_error)
 
 
 def e0_read_status(status, stream=None) -> int:
