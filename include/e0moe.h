@@ -46,10 +46,13 @@
  * e0_slot_bytes(H, I) bytes:
  *     [0, I*H)                 gate/up codes, row-interleaved: for each i the
  *                              gate row i (H/2 bytes) then the up row i
- *     [I*H, I*H + H*I/2)       down codes, [H][I/2]
+ *     [I*H, I*H + H*I/2)       down codes, half-group major: the 16 bytes of
+ *                              row j, inputs 32c..32c+31, at (c*H + j)*16
  *     next I*(H/64)*2*4 bytes  gate/up (scale, bias) fp16 pairs, [I][2][H/64]
- *     next H*(I/64)*4 bytes    down (scale, bias) fp16 pairs, [H][I/64]
- * Codes keep the canonical row order, but inside every 32-bit word (8
+ *     next H*(I/64)*4 bytes    down (scale, bias) fp16 pairs, group major:
+ *                              group g of row j at (g*H + j)*4
+ * (A down slice "rows j0..j1 of half-group c" is one contiguous range, so it
+ * can be fetched with one bulk copy.)  Inside every 32-bit word (8
  * elements e0..e7 of a row) the nibbles are interleaved: nibble j (bits
  * 4j..4j+3, little-endian word) holds e0, e2, e4, e6, e1, e3, e5, e7 for
  * j = 0..7.  Masking a word with 0x000F000F / 0x00F000F0 (and the same after

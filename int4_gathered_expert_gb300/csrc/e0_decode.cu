@@ -34,9 +34,10 @@ __global__ void k_pack_expert(e0_expert_q src, uint8_t* dst, int H, int I, int32
             const uint8_t* s = c < half ? src.gate.codes + i * (H / 2) + c * 16 : src.up.codes + i * (H / 2) + (c - half) * 16;
             *reinterpret_cast<uint4*>(dst + i * H + c * 16) = interleave16(*reinterpret_cast<const uint4*>(s));
         } else if (q < n_gu + n_dn) {
-            const size_t c = q - n_gu;
-            *reinterpret_cast<uint4*>(dst + sl.down_codes() + c * 16) =
-                interleave16(*reinterpret_cast<const uint4*>(src.down.codes + c * 16));
+            // half-group major: chunk (c, j) = row j, inputs 32c..32c+31
+            const size_t q2 = q - n_gu, c = q2 / H, j = q2 % H;
+            *reinterpret_cast<uint4*>(dst + sl.down_codes() + q2 * 16) =
+                interleave16(*reinterpret_cast<const uint4*>(src.down.codes + j * (I / 2) + c * 16));
         } else if (q < n_gu + n_dn + n_gsb) {
             const size_t p = q - n_gu - n_dn;
             const size_t i = p / (2 * GH), which = (p / GH) % 2, g = p % GH;
@@ -44,8 +45,9 @@ __global__ void k_pack_expert(e0_expert_q src, uint8_t* dst, int H, int I, int32
             const uint32_t v = (uint32_t)qt.scale[i * GH + g] | ((uint32_t)qt.bias[i * GH + g] << 16);
             *reinterpret_cast<uint32_t*>(dst + sl.gu_sb() + p * 4) = v;
         } else {
-            const size_t p = q - n_gu - n_dn - n_gsb;
-            const uint32_t v = (uint32_t)src.down.scale[p] | ((uint32_t)src.down.bias[p] << 16);
+            // group major: word (g, j) = group g of row j
+            const size_t p = q - n_gu - n_dn - n_gsb, g = p / H, j = p % H;
+            const uint32_t v = (uint32_t)src.down.scale[j * GI + g] | ((uint32_t)src.down.bias[j * GI + g] << 16);
             *reinterpret_cast<uint32_t*>(dst + sl.down_sb() + p * 4) = v;
         }
     }

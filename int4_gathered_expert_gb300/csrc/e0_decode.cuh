@@ -502,16 +502,16 @@ E0_DEV void phase_down(const DecodeArgs& A, int blk, int nblk, char* smem) {
                     const int s = slots[t * K + k];
                     if (s < 0) continue;
                     const uint8_t* ex = A.L.pool + (size_t)s * sbytes;
-                    const uint8_t* cp = ex + dcode + (size_t)j * (I / 2) + 32 * rm.g;
-                    const uint4 c0 = ldg_stream(cp), c1 = ldg_stream(cp + 16);
-                    const uint32_t sb = ldg_u32(ex + dsb + ((size_t)j * GI + rm.g) * 4);
+                    const uint8_t* cp = ex + dcode + ((size_t)(2 * rm.g) * H + j) * 16;
+                    const uint4 c0 = ldg_stream(cp), c1 = ldg_stream(cp + (size_t)H * 16);
+                    const uint32_t sb = ldg_u32(ex + dsb + ((size_t)rm.g * H + j) * 4);
                     const int pq = (t * NE + k) * GI + rm.g;
                     acc = fmaf(wts[t * K + k], q4_group_dot(c0, c1, planes + pq * 8, xg[pq], sb), acc);
                 }
                 if (sh) {
-                    const uint8_t* cp = A.L.sh + dcode + (size_t)j * (I / 2) + 32 * rm.g;
-                    const uint4 c0 = ldg_stream(cp), c1 = ldg_stream(cp + 16);
-                    const uint32_t sb = ldg_u32(A.L.sh + dsb + ((size_t)j * GI + rm.g) * 4);
+                    const uint8_t* cp = A.L.sh + dcode + ((size_t)(2 * rm.g) * H + j) * 16;
+                    const uint4 c0 = ldg_stream(cp), c1 = ldg_stream(cp + (size_t)H * 16);
+                    const uint32_t sb = ldg_u32(A.L.sh + dsb + ((size_t)rm.g * H + j) * 4);
                     const int pq = (t * NE + NK) * GI + rm.g;
                     acc += q4_group_dot(c0, c1, planes + pq * 8, xg[pq], sb);
                 }

@@ -487,6 +487,14 @@ E0_DEV P2Item p2_item(const GemmP& p, int idx, int MT) {
     return it;
 }
 
+E0_DEV void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y, int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
 E0_DEV void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y, int z) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -546,11 +554,12 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             const uint8_t* sbp = nullptr;
             if (ex) {
                 if (MODE == MODE_GATEUP) sbp = ex + sl.gu_sb() + (size_t)wr * (p.H / GROUP) * 4;
-                else sbp = ex + sl.down_sb() + (size_t)wr * (p.I / GROUP) * 4;
+                else sbp = ex + sl.down_sb() + (size_t)wr * 4;  // group kk at + kk * H * 4
             }
             for (int kk = 0; kk < nk; ++kk, ++g) {
                 const uint32_t s = g % P2_STAGES;
-                const uint32_t sbits = ex ? ldg_u32(sbp + kk * 4) : 0u;
+                const uint32_t sbits =
+                    ex ? ldg_u32(sbp + (MODE == MODE_GATEUP ? (size_t)kk * 4 : (size_t)kk * p.H * 4)) : 0u;
                 if (!mbar_wait(&raw_full[s], (g / P2_STAGES) & 1, abort, WAIT_LIMIT_NS)) {
                     ok = false;
                     *abort = 1;
@@ -559,8 +568,12 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 }
                 uint8_t* st = smem + s * P2_STAGE;
                 if (ex) {
-                    const uint4* rawp = reinterpret_cast<const uint4*>(st + P2_A + P2_B + r * 32);
-                    dequant64_to_tile(rawp[0], rawp[1], sbits, st, r);
+                    // gate/up raw tile: [128 rows][32 B]; down raw tile: [2 half-groups][128 rows][16 B]
+                    const uint8_t* raw = st + P2_A + P2_B;
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 : raw + r * 16);
+                    const uint4 c1 =
+                        *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 + 16 : raw + 2048 + r * 16);
+                    dequant64_to_tile(c0, c1, sbits, st, r);
                 } else {
                     zero_row_of_tile(st, r);
                 }
@@ -629,7 +642,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                     }
                     uint8_t* st = smem + s * P2_STAGE;
                     mbar_arrive_expect_tx(&raw_full[s], P2_RAW + P2_B);
-                    tma_load_3d(&tmCodes, &raw_full[s], st + P2_A + P2_B, kk * 32, it.m * 128, z);
+                    if (MODE == MODE_GATEUP) tma_load_3d(&tmCodes, &raw_full[s], st + P2_A + P2_B, kk * 32, it.m * 128, z);
+                    else tma_load_4d(&tmCodes, &raw_full[s], st + P2_A + P2_B, 0, it.m * 128, 2 * kk, z);
                     tma_load_2d(&tmB, &raw_full[s], st + P2_A, kk * BK, it.row0);
                 }
             }
@@ -892,13 +906,26 @@ static bool make_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uin
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over the down codes of every slot, half-group major: {16 bytes,
+// H rows, I/32 half-groups, slots}; one box = two half-groups (one 64-input
+// K step) of 128 rows, stored [2][128][16 B] in shared memory.
+static bool make_down_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t slots,
+                          uint64_t slot_stride) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {16, H, I / 32, slots};
+    cuuint64_t strides[3] = {16, H * 16, slot_stride};
+    cuuint32_t box[4] = {16, 128, 2, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static std::once_flag g_prefill_init;
 static void prefill_attrs() {
     cudaFuncSetAttribute(k_umma<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)gemm_smem<MODE_ROUTER>());
-    cudaFuncSetAttribute(k_umma<MODE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)gemm_smem<MODE_GATEUP>());
-    cudaFuncSetAttribute(k_umma<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem<MODE_DOWN>());
     cudaFuncSetAttribute(k_umma2<MODE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm2_smem());
     cudaFuncSetAttribute(k_umma2<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm2_smem());
 }
@@ -970,8 +997,8 @@ int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, con
     CUtensorMap mGU, mDN;
     const size_t sbytes = slot_bytes(H, I);
     if (!make_codes_map(&mGU, bank->data, (uint64_t)H / 2, (uint64_t)2 * I, (uint64_t)bank->n_slots, sbytes) ||
-        !make_codes_map(&mDN, bank->data + SlotLayout{H, I}.down_codes(), (uint64_t)I / 2, (uint64_t)H,
-                        (uint64_t)bank->n_slots, sbytes))
+        !make_down_map(&mDN, bank->data + SlotLayout{H, I}.down_codes(), (uint64_t)H, (uint64_t)I,
+                       (uint64_t)bank->n_slots, sbytes))
         return E0_ERR_CUDA;
     gp.K = H;
     gp.rows_out = 2 * I;

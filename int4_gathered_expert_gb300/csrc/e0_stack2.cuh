@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     extern __shared__ __align__(16) char smem[];
     StackHdr& S = *Sp;
     const int H = S.H, I = S.I, E = S.E, K = S.K, Lz = S.L;
-    const int GH = H / GROUP, GI = I / GROUP;
+    const int GH = H / GROUP;
     const int t = S.t;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = T2_THREADS >> 5;
@@ -575,8 +575,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                     const uint8_t* ex = (live && u < sp.u1) ? slot_s[u / sp.HG < K ? u / sp.HG : K] : nullptr;
                     if (ex) {
                         const int hg = u % sp.HG;
-                        cv[q] = ldg_stream(ex + sl.down_codes() + (size_t)j * (I / 2) + hg * 16);
-                        sbv[q] = ldg_u32(ex + sl.down_sb() + ((size_t)j * GI + hg / 2) * 4);
+                        cv[q] = ldg_stream(ex + sl.down_codes() + ((size_t)hg * H + j) * 16);
+                        sbv[q] = ldg_u32(ex + sl.down_sb() + ((size_t)(hg / 2) * H + j) * 4);
                     }
                 }
 #pragma unroll
