@@ -201,7 +201,7 @@ struct StackHdr {
     float* hpre2;        // [2][hidden] head fc1 outputs, by layer parity
     float* zres2;        // [2][E] head linear-residual outputs
     float* z2;           // [2][E] head logits
-    int32_t grid2, smem2, teams;
+    int32_t grid2, smem2, teams, smem2_gu, smem2_dn;
 };
 
 struct TraceP {
@@ -304,7 +304,7 @@ E0_DEV bool layer_native(const StackHdr& S, const LayerP& L, int t) { return t =
 
 // Route the head logits z of owner layer `l` into the prediction consumed by
 // layer l+1 at the next token (one warp).
-E0_DEV void stack_route_head(const StackHdr& S, int l, int t, float* scr, TraceP tr, uint32_t* st, int lane,
+__device__ __noinline__ void stack_route_head(const StackHdr& S, int l, int t, float* scr, TraceP tr, uint32_t* st, int lane,
                              const float* z = nullptr) {
     if (l + 1 >= S.L) return;
     if (z == nullptr) z = S.z;
@@ -321,7 +321,7 @@ E0_DEV void stack_route_head(const StackHdr& S, int l, int t, float* scr, TraceP
 }
 
 // Resolve the routing layer l uses at token t into inds/w (one warp).
-E0_DEV void stack_resolve(const StackHdr& S, const LayerP& L, int l, int t, int32_t* inds, float* w, float* scr,
+__device__ __noinline__ void stack_resolve(const StackHdr& S, const LayerP& L, int l, int t, int32_t* inds, float* w, float* scr,
                           uint32_t* st, int lane) {
     if (layer_native(S, L, t)) {
         route_warp(S.logits, S.E, S.rp, inds, w, scr, st, lane);
@@ -544,6 +544,7 @@ __global__ void __launch_bounds__(PHASE_THREADS) k_stack_token(StackHdr* Sp, con
 // ================================================================== host side
 
 static int g_num_sms = 0;
+static int g_smem_optin = 0;
 static std::once_flag g_init;
 
 static void init_attrs() {
@@ -556,7 +557,15 @@ static void init_attrs() {
     cudaFuncSetAttribute(k_stack_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     cudaFuncSetAttribute(k_stack_down, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     cudaFuncSetAttribute(k_stack_token, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-    cudaFuncSetAttribute(k_stack_token2, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (g_smem_optin <= 0) g_smem_optin = big;
+    cudaFuncSetAttribute(k_stack_token2, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
+}
+
+// largest dynamic shared memory one block of the cluster kernel may take
+static size_t smem_optin() {
+    num_sms();
+    return (size_t)g_smem_optin;
 }
 
 int num_sms() {
@@ -876,15 +885,17 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
     if (per_sm < 1) per_sm = 1;
     if (per_sm > 2) per_sm = 2;
     hdr.grid = num_sms() * per_sm;
-    // cluster kernel geometry: as many 8-CTA teams as can be resident at once
+    // cluster kernel geometry
     {
-        const T2Smem t2(H, E, L, rp->K);
-        hdr.smem2 = (int32_t)t2.total;
+        // teams: as many 8-CTA clusters as can be resident at once with the
+        // largest shared-memory footprint; every team must hold at most
+        // T2_MAX_UNITS half-groups of a layer
+        const size_t limit = smem_optin();
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3((num_sms() / TEAM) * TEAM);
         cfg.blockDim = dim3(T2_THREADS);
-        cfg.dynamicSmemBytes = t2.total;
+        cfg.dynamicSmemBytes = limit;
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
         at[0].val.clusterDim.x = TEAM;
@@ -899,11 +910,35 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
         }
         int teams = num_sms() / TEAM;
         if (ncl < teams) teams = ncl;
-        // every team must hold at most T2_MAX_UNITS half-groups of the layer
-        const int nu = (rp->K + 1) * (I / 32);
-        if (teams > 0 && (nu + teams - 1) / teams > T2_MAX_UNITS) teams = 0;
+        // the largest run of half-group units a team takes, over the layer
+        // configurations of this stack
+        int rank = 0, max_units = 0;
+        for (int l = 0; l < L && teams > 0; ++l) {
+            const bool sh = layers[l].shared != nullptr;
+            const bool heavy = sh && layers[l].shared->A_gate != nullptr;
+            if (heavy && layers[l].shared->rank > rank) rank = layers[l].shared->rank;
+            for (int tau = 0; tau < teams; ++tau) {
+                const T2Split sp(I, rp->K, sh, heavy, tau, teams);
+                if (sp.u1 - sp.u0 > max_units) max_units = sp.u1 - sp.u0;
+            }
+        }
+        if (teams > 0 && max_units > T2_MAX_UNITS) teams = 0;
         hdr.teams = teams;
         hdr.grid2 = teams * TEAM;
+        // staging regions: what one member needs per layer, as far as the
+        // shared memory allows
+        size_t gu = 0, dn = 0;
+        stage_need(H, I, max_units > 0 ? max_units : 1, rank, &gu, &dn);
+        gu = (gu + 127) & ~(size_t)127;
+        dn = (dn + 127) & ~(size_t)127;
+        const size_t base = T2Smem(H, E, L, rp->K, 0, 0).total;
+        // two down regions; the down side gives way first, then the gate/up side
+        if (base + gu + 2 * dn > limit) dn = base + gu < limit ? (((limit - base - gu) / 2) & ~(size_t)127) : 0;
+        if (base + gu + 2 * dn > limit) gu = base < limit ? ((limit - base) & ~(size_t)127) : 0;
+        const T2Smem t2(H, E, L, rp->K, gu, dn);
+        hdr.smem2 = (int32_t)t2.total;
+        hdr.smem2_gu = (int32_t)gu;
+        hdr.smem2_dn = (int32_t)dn;
     }
     LayerP* hl = new LayerP[L];
     for (int l = 0; l < L; ++l)

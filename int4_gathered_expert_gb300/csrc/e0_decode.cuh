@@ -189,7 +189,7 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
     }
 }
 
-E0_DEV void route_warp(const float* lg, int E, const RouteP& rp, int32_t* inds, float* w, float* scr, uint32_t* st,
+static __device__ __noinline__ void route_warp(const float* lg, int E, const RouteP& rp, int32_t* inds, float* w, float* scr, uint32_t* st,
                        int lane) {
     if (E <= 32) route_warp_t<1>(lg, E, rp, inds, w, scr, st, lane);
     else if (E <= 64) route_warp_t<2>(lg, E, rp, inds, w, scr, st, lane);

@@ -28,7 +28,6 @@
 
 constexpr int TEAM = 8;             // CTAs per cluster
 constexpr int T2_THREADS = 384;     // 12 warps
-constexpr int T2_EXPERT_WARPS = 12; // warps 0..11: experts; 12..15: head and bookkeeping
 constexpr int T2_MAX_UNITS = 32;    // half-groups per team
 constexpr int T2_MAX_RANK = 64;
 
@@ -89,13 +88,15 @@ E0_DEV void prefetch_share(const void* base, size_t bytes, int b, int n) {
 
 // ------------------------------------------------------------------ barrier
 
-// Grid barrier on a 64-bit monotonic counter: arrive with a release add,
-// wait with acquire loads until the counter reaches the target; gives up
-// after a bounded number of polls (or when another CTA already did),
-// raising E0_ST_TIMEOUT.
-E0_DEV void grid_barrier2(StackHdr* S, unsigned long long target, uint32_t* st) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
+// Grid barrier in two levels: the CTAs of a team meet at a cluster barrier
+// (everything they wrote before it is then ordered before the team leader's
+// release), one thread per team arrives on the monotonic counter with a
+// release add and waits with acquire loads until every team has arrived,
+// then the team meets again.  The wait is bounded: after 2^24 polls, or
+// once another team gave up (abort flag), it stops and raises E0_ST_TIMEOUT.
+E0_DEV void grid_barrier_team(StackHdr* S, unsigned long long target, uint32_t* st) {
+    cl_sync();
+    if (threadIdx.x == 0 && cl_rank() == 0) {
         __threadfence();
         asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(&S->bar_ctr), "l"(1ull) : "memory");
         uint32_t it = 0;
@@ -113,7 +114,7 @@ E0_DEV void grid_barrier2(StackHdr* S, unsigned long long target, uint32_t* st) 
             }
         }
     }
-    __syncthreads();
+    cl_sync();
 }
 
 // ------------------------------------------------------------------ quantise / dot (32-element half-groups)
@@ -186,17 +187,17 @@ E0_DEV float h8_dot44(const uint4 wv, const float4 a, const float4 b) {
 // 256, so one load of the warp covers 512 contiguous bytes of the row and the
 // shared-memory reads of neighbouring lanes do not collide.  Sum the lanes
 // with warp_sum.
-__device__ __noinline__ float hrow_dot(const __half* w, const float* x, int n, int lane) {
+E0_DEV float hrow_dot(const __half* w, const float* x, int n, int lane) {
     float acc = 0.f;
-    for (int c0 = 0; c0 < n; c0 += 4 * 256) {
-        uint4 wv[4];
+    for (int c0 = 0; c0 < n; c0 += 8 * 256) {
+        uint4 wv[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
             const int c = c0 + k * 256 + lane * 8;
             if (c < n) wv[k] = ldg_stream(w + c);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
             const int c = c0 + k * 256 + lane * 8;
             if (c < n)
                 acc += h8_dot44(wv[k], *reinterpret_cast<const float4*>(x + c), *reinterpret_cast<const float4*>(x + c + 4));
@@ -234,14 +235,338 @@ __device__ __noinline__ float hrow_dot_gelu(const __half* w, const float* hp, in
     return acc;
 }
 
+// Up to four consecutive fp16 rows (row stride ld halves) of the head's second
+// layer times gelu_erf(hp), hp written by other blocks earlier in the launch
+// (read from L2); the activation is evaluated once for all rows.
+E0_DEV void hrow_dot_gelu4(const __half* w, size_t ld, int nrows, const float* hp, int n, int lane,
+                                            float* acc) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c0 = 0; c0 < n; c0 += 2 * 256) {
+        uint4 wv[4][2];
+        float4 a[2], b[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int c = c0 + k * 256 + lane * 8;
+            if (c < n) {
+                a[k] = __ldcg(reinterpret_cast<const float4*>(hp + c));
+                b[k] = __ldcg(reinterpret_cast<const float4*>(hp + c + 4));
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (q < nrows) wv[q][k] = ldg_stream(w + (size_t)q * ld + c);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int c = c0 + k * 256 + lane * 8;
+            if (c < n) {
+                const float4 ga = make_float4(gelu_erf_f(a[k].x), gelu_erf_f(a[k].y), gelu_erf_f(a[k].z), gelu_erf_f(a[k].w));
+                const float4 gb = make_float4(gelu_erf_f(b[k].x), gelu_erf_f(b[k].y), gelu_erf_f(b[k].z), gelu_erf_f(b[k].w));
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (q < nrows) s[q] += h8_dot44(wv[q][k], ga, gb);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = s[q];
+}
+
+// ------------------------------------------------------------------ staging of weight slices
+
+constexpr int T2_EXPERT_W = 8;   // warps 0..7: experts; 8..11: prerouter heads and staging
+constexpr int T2_GU_BATCH = 2;  // gate/up rows a warp loads before it computes
+constexpr int T2_MAX_SEG = 4;    // gate/up row runs of one member (one per expert touched)
+
+constexpr int T2_STAGE_RANK = 16;   // LoRA ranks up to this are staged; larger ones read global memory
+constexpr int T2_STAGE_ROUNDS = 3;  // up to 96 ranges per side and layer
+constexpr int T2_STAGE_MAX = 32 * T2_STAGE_ROUNDS;
+
+// Sources of a staged range: the slots of the K routed experts (0..K-1) and of
+// the shared expert (K), then the LoRA matrices.
+enum { SRC_AG = 1, SRC_AU, SRC_BG, SRC_BU, SRC_AD, SRC_BD };  // added to K
+
+// One range of a layer's weights: `bytes` at byte offset `off` from source
+// `kind`, copied to byte `soff` of the staging region (soff < 0: read in place).
+struct StageEnt {
+    uint64_t off;
+    uint32_t bytes;
+    int32_t kind;
+    int32_t soff;
+    int32_t pad;
+};
+
+// The ranges of one side of a layer for this member.  They depend only on the
+// layer's configuration (shared expert or not, LoRA staged or not), not on
+// its routing, so they are laid out once per configuration.
+struct StageTab {
+    int cfg;  // configuration the table was built for (-1: none yet)
+    int n;
+    StageEnt e[T2_STAGE_MAX];
+};
+
+// Where this CTA's weight slices of a layer are read from (a staging region of
+// shared memory, or global memory), in the order of the tables.  Gate/up side
+// (one region, one layer at a time): 2 * n_gu pointers for the row runs
+// (codes, (scale, bias)), 2 * ra rows of LoRA A_gate then A_up (from the
+// member's first column), then LoRA B_gate, B_up from the member's first
+// shared row (when bsh).  Down side (two regions, by layer parity): 2 * nu
+// pointers for the down slices (codes, (scale, bias)), rd rows of LoRA A_down
+// (from the team's first shared column), then LoRA B_down from the member's
+// first output row (when rd > 0).
+struct StagePlan {
+    StageTab gut, dnt;
+    int n_gu, gu_pos[T2_MAX_SEG + 1], ra, bsh;  // gu_pos: first team position of each run; [n_gu] = end
+    const uint8_t* gu[T2_STAGE_MAX];
+    int dn_nu, dn_rd;  // of the down table
+    int nu[2], rd[2];  // of the layer each down region holds
+    const uint8_t* dn[2][T2_STAGE_MAX];
+    E0_DEV const uint8_t* gu_codes(int n) const { return gu[2 * n]; }
+    E0_DEV const uint8_t* gu_sb(int n) const { return gu[2 * n + 1]; }
+    E0_DEV const __half* ag(int q) const { return ra ? reinterpret_cast<const __half*>(gu[2 * n_gu + q]) : nullptr; }
+    E0_DEV const __half* bg() const { return bsh ? reinterpret_cast<const __half*>(gu[2 * n_gu + 2 * ra]) : nullptr; }
+    E0_DEV const __half* bu() const { return bsh ? reinterpret_cast<const __half*>(gu[2 * n_gu + 2 * ra + 1]) : nullptr; }
+    E0_DEV const uint8_t* dn_codes(int b, int u) const { return dn[b][2 * u]; }
+    E0_DEV const uint8_t* dn_sb(int b, int u) const { return dn[b][2 * u + 1]; }
+    E0_DEV const __half* ad(int b, int q) const {
+        return rd[b] ? reinterpret_cast<const __half*>(dn[b][2 * nu[b] + q]) : nullptr;
+    }
+    E0_DEV const __half* bd(int b) const {
+        return rd[b] ? reinterpret_cast<const __half*>(dn[b][2 * nu[b] + rd[b]]) : nullptr;
+    }
+};
+
+E0_DEV void fence_async_smem2() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+E0_DEV void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(bytes), "r"((uint32_t)__cvta_generic_to_shared(bar))
+                 : "memory");
+}
+E0_DEV void mbar_init2(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(bar)), "r"(count)
+                 : "memory");
+}
+E0_DEV void mbar_expect2(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Bounded wait for a staging barrier's phase; false when it gave up.
+E0_DEV bool mbar_wait2(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
+    for (uint32_t it = 0; it < (1u << 22); ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// Lays out the ranges of one side (item(i) gives range i as {kind, off,
+// bytes}): taken in order while the running total of stageable bytes fits in
+// cap; a range that is not whole 16-byte chunks at a 16-byte offset, or that
+// comes after the region is full, is read in place.  One warp.
+template <class Item>
+E0_DEV void stage_layout(StageTab* tab, int cfg, int n, Item item, size_t cap, int lane) {
+    uint32_t base = 0;
+    for (int r = 0; r < T2_STAGE_ROUNDS; ++r) {
+        const int i = r * 32 + lane;
+        StageEnt e{0ull, 0u, -1, -1, 0};
+        if (i < n) item(i, e);
+        const bool ok = i < n && e.bytes > 0 && !(e.bytes & 15u) && !(e.off & 15ull);
+        const uint32_t sz = ok ? e.bytes : 0u;
+        uint32_t inc = sz;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        e.soff = (ok && (size_t)base + inc <= cap) ? (int32_t)(base + inc - sz) : -1;
+        base += __shfl_sync(0xffffffffu, inc, 31);
+        if (i < n) tab->e[i] = e;
+    }
+    if (lane == 0) {
+        tab->n = n;
+        tab->cfg = cfg;
+    }
+    __syncwarp();
+}
+
+// Issues one side of a layer from its table: slots[0..K] and the LoRA
+// matrices are the layer's sources; rec[i] receives where range i is read from.  One warp; completes on
+// `bar` with one arrival plus the bytes copied.  Every record happens before
+// the arrival.
+struct LoraPtrs {
+    const __half *Ag, *Au, *Bg, *Bu, *Ad, *Bd;
+};
+
+E0_DEV void stage_issue(const StageTab* tab, const uint8_t* const* slots, int K, const LoraPtrs& lo, uint8_t* buf,
+                        const uint8_t** rec, uint64_t* bar, int lane) {
+    const uint8_t* from[T2_STAGE_ROUNDS];
+    int32_t to[T2_STAGE_ROUNDS];
+    uint32_t nbytes[T2_STAGE_ROUNDS];
+    uint32_t tot = 0;
+    const int n = tab->n;
+#pragma unroll
+    for (int r = 0; r < T2_STAGE_ROUNDS; ++r) {
+        const int i = r * 32 + lane;
+        from[r] = nullptr;
+        to[r] = -1;
+        nbytes[r] = 0;
+        if (i < n) {
+            const StageEnt e = tab->e[i];
+            const void* bv = nullptr;
+            switch (e.kind - K) {
+                case SRC_AG: bv = lo.Ag; break;
+                case SRC_AU: bv = lo.Au; break;
+                case SRC_BG: bv = lo.Bg; break;
+                case SRC_BU: bv = lo.Bu; break;
+                case SRC_AD: bv = lo.Ad; break;
+                case SRC_BD: bv = lo.Bd; break;
+                default: bv = slots[e.kind];
+            }
+            const uint8_t* b = reinterpret_cast<const uint8_t*>(bv);
+            const uint8_t* p = b ? b + e.off : nullptr;
+            const bool cp = p && e.soff >= 0 && !(reinterpret_cast<uintptr_t>(p) & 15u);
+            rec[i] = cp ? buf + e.soff : p;
+            if (cp) {
+                from[r] = p;
+                to[r] = e.soff;
+                nbytes[r] = e.bytes;
+                tot += e.bytes;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    // the region's previous contents were read by the generic proxy
+    fence_async_smem2();
+    __syncwarp();
+    if (lane == 0) mbar_expect2(bar, tot);
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < T2_STAGE_ROUNDS; ++r)
+        if (to[r] >= 0) bulk_copy(buf + to[r], from[r], nbytes[r], bar);
+}
+
+// Gate/up side: the row runs of team positions [p0, p1) (one run per expert
+// touched; consecutive positions of one expert are consecutive rows of its
+// slot: codes, then (scale, bias) words), the member's column slice
+// [c0, c0 + nc) of the ra rows of LoRA A_gate and A_up, and the LoRA B_gate /
+// B_up rows of its shared-expert positions [ps, p1) (first row i_s).
+__device__ __noinline__ void stage_layout_gu(StagePlan* plan, int cfg, const SlotLayout& sl, int H, int K, int HG,
+                                             int u0, int p0, int p1, int ra, int rank, int c0, int nc, int ps, int i_s,
+                                             size_t cap, int lane) {
+    const int GH = H / GROUP;
+    const int ke0 = (u0 + p0 / 32) / HG;
+    const int nrun = p1 > p0 ? (u0 + (p1 - 1) / 32) / HG - ke0 + 1 : 0;
+    const int n_gu = nrun < T2_MAX_SEG ? nrun : T2_MAX_SEG;
+    const bool bsh = ra > 0 && ps < p1;
+    auto run_start = [&](int n) { return max(p0, ((ke0 + n) * HG - u0) * 32); };
+    auto run_end = [&](int n) { return min(p1, ((ke0 + n + 1) * HG - u0) * 32); };
+    auto item = [&](int i, StageEnt& e) {
+        if (i < 2 * n_gu) {
+            const int n = i >> 1;
+            const int pst = run_start(n), rows = run_end(n) - pst;
+            const int ia = ((u0 + pst / 32) % HG) * 32 + pst % 32;
+            e.kind = min(ke0 + n, K);
+            if (i & 1) {
+                e.off = sl.gu_sb() + (uint64_t)ia * 2 * GH * 4;
+                e.bytes = (uint32_t)rows * 2 * GH * 4;
+            } else {
+                e.off = (uint64_t)ia * H;
+                e.bytes = (uint32_t)rows * H;
+            }
+            return;
+        }
+        const int q = i - 2 * n_gu;
+        if (q < 2 * ra) {
+            e.kind = K + (q < ra ? SRC_AG : SRC_AU);
+            e.off = ((uint64_t)(q % ra) * H + c0) * 2;
+            e.bytes = (uint32_t)nc * 2;
+            return;
+        }
+        e.kind = K + (q == 2 * ra ? SRC_BG : SRC_BU);
+        e.off = (uint64_t)i_s * rank * 2;
+        e.bytes = (uint32_t)(p1 - ps) * rank * 2;
+    };
+    if (lane == 0) {
+        plan->n_gu = n_gu;
+        for (int n = 0; n < n_gu; ++n) plan->gu_pos[n] = run_start(n);
+        plan->gu_pos[n_gu] = n_gu > 0 ? run_end(n_gu - 1) : p0;
+        plan->ra = ra;
+        plan->bsh = bsh ? 1 : 0;
+    }
+    stage_layout(&plan->gut, cfg, 2 * n_gu + 2 * ra + (bsh ? 2 : 0), item, cap, lane);
+}
+
+// Down side: the down slices (output rows [j0, j1)) of half-group units
+// [u0, u1), the team's shared columns [i0, i0 + ni) of the rd rows of LoRA
+// A_down, and the member's rows of LoRA B_down.
+__device__ __noinline__ void stage_layout_dn(StagePlan* plan, int cfg, const SlotLayout& sl, int H, int K, int HG,
+                                             int u0, int u1, int j0, int j1, int rd, int rank, int i0, int ni,
+                                             size_t cap, int lane) {
+    const int nu = u1 - u0;
+    auto item = [&](int i, StageEnt& e) {
+        if (i < 2 * nu) {
+            const int u = u0 + (i >> 1), hg = u % HG;
+            e.kind = min(u / HG, K);
+            if (i & 1) {
+                e.off = sl.down_sb() + ((uint64_t)(hg / 2) * H + j0) * 4;
+                e.bytes = (uint32_t)(j1 - j0) * 4;
+            } else {
+                e.off = sl.down_codes() + ((uint64_t)hg * H + j0) * 16;
+                e.bytes = (uint32_t)(j1 - j0) * 16;
+            }
+            return;
+        }
+        const int q = i - 2 * nu;
+        if (q < rd) {
+            e.kind = K + SRC_AD;
+            e.off = ((uint64_t)q * (HG * 32) + i0) * 2;
+            e.bytes = (uint32_t)ni * 2;
+            return;
+        }
+        e.kind = K + SRC_BD;
+        e.off = (uint64_t)j0 * rank * 2;
+        e.bytes = (uint32_t)(j1 - j0) * rank * 2;
+    };
+    if (lane == 0) {
+        plan->dn_nu = nu;
+        plan->dn_rd = rd;
+    }
+    stage_layout(&plan->dnt, cfg, 2 * nu + (rd > 0 ? rd + 1 : 0), item, cap, lane);
+}
+
+// Bytes one member may stage for one layer when NT teams share nk experts:
+// gate/up rows (codes + scale/bias) and down slices.
+__host__ __device__ inline void stage_need(int H, int I, int units, int rank, size_t* gu, size_t* dn) {
+    const int rows = (units * 32 + TEAM - 1) / TEAM;
+    const int r = rank <= T2_STAGE_RANK ? rank : 0;
+    *gu = (size_t)rows * (H + 2 * (H / GROUP) * 4) + (size_t)T2_MAX_SEG * 64  // row runs
+          + (size_t)2 * r * (H / TEAM) * 2 + (size_t)2 * rows * r * 2;       // LoRA A slices, B rows
+    *dn = (size_t)units * (H / TEAM) * 20                                     // down slices
+          + (size_t)r * units * 32 * 2 + (size_t)(H / TEAM) * r * 2;          // LoRA A_down, B_down
+}
+
 // ------------------------------------------------------------------ shared memory layout
 
 struct T2Smem {
-    size_t r, h, hpl, hxg, ateam, apl, axg, zred, zg, zu, zd, inds, w, slots, scr, red, total;
-    __host__ __device__ T2Smem(int H, int E, int L, int K) {
+    size_t hdr, lyr, r, h, hpl, hxg, ateam, apl, axg, zred, zg, zu, zd, inds, w, slots, scr, red, hnext, plan, bars, stage_gu,
+        stage_dn, dn_bytes, total;
+    __host__ __device__ T2Smem(int H, int E, int L, int K, size_t gu_cap, size_t dn_cap) {
         const int GH = H / GROUP;
         const int max_rows = T2_MAX_UNITS * 32;
         size_t o = 0;
+        hdr = o;  // copy of the stack header (read-only during a launch)
+        o += (sizeof(StackHdr) + 15) & ~(size_t)15;
+        lyr = o;  // copy of the layer descriptors
+        o += ((size_t)L * sizeof(LayerP) + 15) & ~(size_t)15;
         r = o;
         o += (size_t)H * 4;
         h = o;
@@ -276,53 +601,80 @@ struct T2Smem {
         o += (size_t)2 * E * 4;
         red = o;
         o += 32 * 4;
+        hnext = o;  // next prerouter-head unit of this block
+        o += 16;
+        o = (o + 15) & ~(size_t)15;
+        plan = o;
+        o += sizeof(StagePlan);
+        o = (o + 15) & ~(size_t)15;
+        bars = o;  // [0] gate/up region, [1], [2] down regions
+        o += 3 * 8;
+        o = (o + 127) & ~(size_t)127;
+        stage_gu = o;
+        o += gu_cap;
+        o = (o + 127) & ~(size_t)127;
+        stage_dn = o;  // two regions of dn_cap bytes, by layer parity
+        dn_bytes = dn_cap;
+        o += 2 * dn_cap;
         total = (o + 127) & ~(size_t)127;
     }
 };
 
-// Work split of one layer: NU half-group units (routed experts first, then the
-// shared expert), team tau of NT takes units [u0, u1).
+// Work split of one layer: NU half-group units (the nk_r routed experts
+// first, then the shared expert when there is one), cut into NT contiguous
+// runs of about equal cost; team tau takes units [u0, u1).  A unit of a shared
+// expert with LoRA costs twice a routed one (its team also computes the LoRA
+// A and B products and waits for one more team exchange), so such teams get
+// fewer units.
 struct T2Split {
     int HG, NU, u0, u1, rows;
-    E0_DEV T2Split(int I, int nk, int tau, int NT) {
+    __host__ __device__ static int bound(int HG, int KH, int NU, bool heavy, int tau, int NT) {
+        if (!heavy) return (int)((long)tau * NU / NT);
+        const long Wt = 2L * KH + 4L * (NU - KH);  // cost in half units
+        const long w = (long)tau * Wt / NT;
+        return w <= 2L * KH ? (int)(w / 2) : KH + (int)((w - 2L * KH) / 4);
+    }
+    // nk_r routed experts; sh: a shared expert follows; heavy: it carries LoRA
+    __host__ __device__ T2Split(int I, int nk_r, bool sh, bool heavy, int tau, int NT) {
         HG = I / 32;
-        NU = nk * HG;
-        u0 = (int)((long)tau * NU / NT);
-        u1 = (int)((long)(tau + 1) * NU / NT);
+        const int KH = nk_r * HG;
+        NU = KH + (sh ? HG : 0);
+        u0 = bound(HG, KH, NU, sh && heavy, tau, NT);
+        u1 = bound(HG, KH, NU, sh && heavy, tau + 1, NT);
         rows = (u1 - u0) * 32;
     }
 };
-
-E0_DEV void prefetch_line(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
-
-// This CTA's share (1/n) of a byte range, prefetched into L2 one 128-byte
-// line per thread and step.
-E0_DEV void prefetch_share_lines(const void* base, size_t bytes, int b, int n) {
-    if (!base || bytes == 0) return;
-    const size_t lines = (bytes + 127) / 128;
-    const size_t per = (lines + n - 1) / n;
-    const size_t l0 = (size_t)b * per, l1 = l0 + per < lines ? l0 + per : lines;
-    const char* c = reinterpret_cast<const char*>(base);
-    for (size_t q = l0 + threadIdx.x; q < l1; q += T2_THREADS) prefetch_line(c + q * 128);
-}
 
 // ------------------------------------------------------------------ the kernel
 
 __global__ void __launch_bounds__(T2_THREADS, 1)
     k_stack_token2(StackHdr* Sp, const float* x, float* r_out, TraceP tr, uint32_t* st) {
     extern __shared__ __align__(16) char smem[];
-    StackHdr& S = *Sp;
-    const int H = S.H, I = S.I, E = S.E, K = S.K, Lz = S.L;
+    const int H = Sp->H, I = Sp->I, E = Sp->E, K = Sp->K, Lz = Sp->L;
     const int GH = H / GROUP;
-    const int t = S.t;
+    const int t = Sp->t;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = T2_THREADS >> 5;
     const int nb = gridDim.x, b = blockIdx.x;
     const int team = (int)cl_id(), NT = (int)cl_count(), crank = (int)cl_rank();
-    const unsigned long long bar0 = S.bar_base;
+    const unsigned long long bar0 = Sp->bar_base;
     int nbar = 0;
 
-    const T2Smem lay(H, E, Lz, K);
+    const T2Smem lay(H, E, Lz, K, (size_t)Sp->smem2_gu, (size_t)Sp->smem2_dn);
+    // The header and the layer descriptors do not change during a launch:
+    // read them from shared memory.  Sp stays the place for the barrier
+    // counters and the end-of-token bookkeeping.
+    {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(Sp);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(smem + lay.hdr);
+        for (int i = threadIdx.x; i < (int)(sizeof(StackHdr) / 4); i += T2_THREADS) dst[i] = src[i];
+        const uint32_t* ls = reinterpret_cast<const uint32_t*>(Sp->layers);
+        uint32_t* ld = reinterpret_cast<uint32_t*>(smem + lay.lyr);
+        for (int i = threadIdx.x; i < (int)((size_t)Lz * sizeof(LayerP) / 4); i += T2_THREADS) ld[i] = ls[i];
+        __syncthreads();
+    }
+    const StackHdr& S = *reinterpret_cast<const StackHdr*>(smem + lay.hdr);
+    const LayerP* lyr = reinterpret_cast<const LayerP*>(smem + lay.lyr);
     float* r = reinterpret_cast<float*>(smem + lay.r);
     float* h = reinterpret_cast<float*>(smem + lay.h);
     uint4* hpl = reinterpret_cast<uint4*>(smem + lay.hpl);
@@ -339,14 +691,29 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     const uint8_t** slot_all = reinterpret_cast<const uint8_t**>(smem + lay.slots);
     float* scr = reinterpret_cast<float*>(smem + lay.scr);
     float* red = reinterpret_cast<float*>(smem + lay.red);
+    int* hnext = reinterpret_cast<int*>(smem + lay.hnext);
+    StagePlan& plan = *reinterpret_cast<StagePlan*>(smem + lay.plan);
+    uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + lay.bars);
+    uint8_t* stage_gu_buf = reinterpret_cast<uint8_t*>(smem + lay.stage_gu);
+    uint8_t* stage_dn_buf = reinterpret_cast<uint8_t*>(smem + lay.stage_dn);
 
     const SlotLayout sl{H, I};
     const size_t sbytes = sl.bytes();
+    const int rows_m = H / TEAM;  // output rows of this member
+    const int j0 = crank * rows_m, j1 = j0 + rows_m;
 
+    if (tid == 0) {
+        mbar_init2(&sbar[0], 1);
+        mbar_init2(&sbar[1], 1);
+        mbar_init2(&sbar[2], 1);
+        plan.gut.cfg = -1;
+        plan.dnt.cfg = -1;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     // ---- routing of every layer that takes a prediction this token (known now)
     for (int q = tid; q < Lz * (K + 1); q += T2_THREADS) {
         const int l = q / (K + 1), k = q % (K + 1);
-        const LayerP& L = S.layers[l];
+        const LayerP& L = lyr[l];
         if (k == K) {
             slot_all[q] = L.sh;
             continue;
@@ -361,13 +728,71 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     }
     __syncthreads();
 
+    auto split_of = [&](int l) {
+        const LayerP& Lq = lyr[l];
+        return T2Split(I, K, Lq.sh != nullptr, Lq.sh != nullptr && Lq.Ag != nullptr, team, NT);
+    };
+    // Staging.  The gate/up region holds one layer at a time and completes once
+    // per layer (layer l waits on parity l & 1); the down regions alternate by
+    // layer parity (layer l waits on region l & 1, parity (l >> 1) & 1).  A
+    // layer whose routing is known when the token starts is copied while the
+    // layer before it runs: its down side when that layer starts, its gate/up
+    // side once that layer's gate/up rows have been read.  A native layer is
+    // copied right after its routing.  The first head warp issues every copy.
+    constexpr int HW = T2_EXPERT_W;
+    // configuration key of a layer's tables: no shared expert; shared expert
+    // with LoRA read in place; shared expert with LoRA of rank r staged
+    auto cfg_of = [&](int l) {
+        const LayerP& Lq = lyr[l];
+        if (!Lq.sh) return 0;
+        return (Lq.Ag && Lq.rank <= T2_STAGE_RANK) ? 2 + Lq.rank : 1;
+    };
+    auto lora_ptrs = [&](int l) {
+        const LayerP& Lq = lyr[l];
+        return LoraPtrs{Lq.Ag, Lq.Au, Lq.Bg, Lq.Bu, Lq.Ad, Lq.Bd};
+    };
+    auto stage_gu_for = [&](int l) {
+        const int cfg = cfg_of(l);
+        if (plan.gut.cfg != cfg) {
+            const T2Split sp = split_of(l);
+            const int p0 = (int)((long)crank * sp.rows / TEAM), p1 = (int)((long)(crank + 1) * sp.rows / TEAM);
+            const int ps = max(p0, (K * sp.HG - sp.u0) * 32);
+            const int i_s = ps < p1 ? ((sp.u0 + ps / 32) % sp.HG) * 32 + ps % 32 : 0;
+            const int ra = (cfg >= 2 && sp.u1 > K * sp.HG) ? cfg - 2 : 0;
+            stage_layout_gu(&plan, cfg, sl, H, K, sp.HG, sp.u0, p0, p1, ra, cfg - 2, crank * (H / TEAM), H / TEAM, ps,
+                            i_s, lay.stage_dn - lay.stage_gu, lane);
+        }
+        stage_issue(&plan.gut, slot_all + l * (K + 1), K, lora_ptrs(l), stage_gu_buf, plan.gu, &sbar[0], lane);
+    };
+    auto stage_dn_for = [&](int l) {
+        const int cfg = cfg_of(l);
+        if (plan.dnt.cfg != cfg) {
+            const T2Split sp = split_of(l);
+            const int us0 = max(sp.u0, K * sp.HG);
+            const int ni = sp.u1 > us0 ? (sp.u1 - us0) * 32 : 0;
+            const int rd = (cfg >= 2 && ni > 0) ? cfg - 2 : 0;
+            stage_layout_dn(&plan, cfg, sl, H, K, sp.HG, sp.u0, sp.u1, j0, j1, rd, cfg - 2, (us0 - K * sp.HG) * 32, ni,
+                            lay.dn_bytes, lane);
+        }
+        const int b = l & 1;
+        if (lane == 0) {
+            plan.nu[b] = plan.dn_nu;
+            plan.rd[b] = plan.dn_rd;
+        }
+        stage_issue(&plan.dnt, slot_all + l * (K + 1), K, lora_ptrs(l), stage_dn_buf + (size_t)b * lay.dn_bytes,
+                    plan.dn[b], &sbar[1 + b], lane);
+    };
+    if (warp == HW && !layer_native(S, lyr[0], t)) {
+        stage_gu_for(0);
+        stage_dn_for(0);
+    }
+
     for (int l = 0; l < Lz; ++l) {
-        const LayerP L = S.layers[l];
+        const LayerP& L = lyr[l];
         const bool native = layer_native(S, L, t);
         const bool sh = L.sh != nullptr;
         const bool lora = sh && L.Ag != nullptr;
         const int rank = lora ? L.rank : 0;
-        const int nk = K + (sh ? 1 : 0);
         int32_t* inds_s = inds_all + l * K;
         float* w_s = w_all + l * K;
         const uint8_t** slot_s = slot_all + l * (K + 1);
@@ -400,6 +825,13 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             for (int j = tid; j < H; j += T2_THREADS) h[j] = r[j] / denom;
             if (b == 0 && tr.r)
                 for (int j = tid; j < H; j += T2_THREADS) tr.r[(size_t)l * H + j] = r[j];
+            // this block's prerouter-head units of layer l start from the first
+            if (tid == 0) {
+                const LayerP& P0 = l >= 1 ? lyr[l - 1] : L;
+                const int nA0 = ((l >= 1 && P0.fc1) ? E : 0) + 3;
+                const int nall = nA0 / 4 + (L.fc1 ? L.hidden + E : 0);
+                *hnext = (int)((long)b * nall / nb);
+            }
             // the output buffer of layer l+1 starts at zero
             if (b == nb - 1)
                 for (int j = tid; j < H; j += T2_THREADS) S.y_acc[(size_t)((l + 1) % 3) * H + j] = 0.f;
@@ -412,7 +844,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                 const float acc = warp_sum(hrow_dot(L.W_r + (size_t)e * H, h, H, lane));
                 if (lane == 0) S.logits[e] = acc;
             }
-            grid_barrier2(Sp, bar0 + (unsigned long long)(++nbar) * nb, st);
+            grid_barrier_team(Sp, bar0 + (unsigned long long)(++nbar) * NT, st);
             if (warp == 0) {
                 stack_resolve(S, L, l, t, inds_s, w_s, scr, b == 0 ? st : nullptr, lane);
                 if (lane < K) {
@@ -422,6 +854,10 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                 }
             }
             __syncthreads();  // warp 0's routing is read by every warp below
+            if (warp == HW) {
+                stage_gu_for(l);
+                stage_dn_for(l);
+            }
         }
         if (b == 0 && warp == 1 && lane < K) {
             const int e = inds_s[lane];
@@ -436,18 +872,25 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         for (int g = warp; g < GH; g += NW) quantize_group_warp(h + GROUP * g, hpl + g, hxg + g, lane, nullptr, GH);
         __syncthreads();
 
-        const T2Split sp(I, nk, team, NT);
+        const T2Split sp = split_of(l);
         const int p0 = (int)((long)crank * sp.rows / TEAM), p1 = (int)((long)(crank + 1) * sp.rows / TEAM);
         const bool team_lora = lora && sp.u1 > K * sp.HG;
+        const bool next_known = l + 1 < Lz && !layer_native(S, lyr[l + 1], t);
+        const int ps_m = max(p0, (K * sp.HG - sp.u0) * 32);  // this member's first shared-expert position
+        const int db = l & 1;  // down region of this layer
 
         // ---- LoRA A of the shared expert (teams holding shared rows): each
         // member reduces 1/TEAM of the inputs, partial sums exchanged
         if (team_lora) {
             const int c0 = crank * (H / TEAM), nc = H / TEAM;
+            if (!mbar_wait2(&sbar[0], l & 1)) set_status(st, E0_ST_TIMEOUT);
             for (int rr = warp; rr < 2 * rank; rr += NW) {
-                const __half* Am = (rr < rank ? L.Ag : L.Au) + (size_t)(rr % rank) * H + c0;
+                const __half* Am =
+                    plan.ag(0) ? plan.ag(rr) : (rr < rank ? L.Ag : L.Au) + (size_t)(rr % rank) * H + c0;
                 float acc = 0.f;
-                for (int c = lane * 8; c < nc; c += 256) acc += h8_dot(ldg_stream(Am + c), h + c0 + c);
+                // Am may point into a staging region: a generic load serves either space
+                for (int c = lane * 8; c < nc; c += 256)
+                    acc += h8_dot(*reinterpret_cast<const uint4*>(Am + c), h + c0 + c);
                 acc = warp_sum(acc);
                 if (lane < TEAM) cl_st(cl_map(zred + crank * 2 * T2_MAX_RANK + rr, lane), acc);
             }
@@ -460,40 +903,58 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             __syncthreads();
         }
 
-        // ---- gate/up rows of this member (all warps), a = silu(G h) * (U h),
-        // stored into every member of the team
-        {
+        if (warp < T2_EXPERT_W) {
+            if (!mbar_wait2(&sbar[0], l & 1)) set_status(st, E0_ST_TIMEOUT);
+            // ---- gate/up rows of this member, a = silu(G h) * (U h), stored into every member
             const RowMap rm(H, lane);
-            const int step = NW * rm.R;
-            for (int pb = p0 + warp * rm.R; pb < p1; pb += 2 * step) {
-                uint4 c[2][4];
-                uint32_t sbv[2][2];
-                const uint8_t* exs[2];
-                int is[2], kes[2];
-                bool lv[2];
+            const int step = T2_EXPERT_W * rm.R;
+            for (int pb = p0 + warp * rm.R; pb < p1; pb += T2_GU_BATCH * step) {
+                uint4 c[T2_GU_BATCH][4];
+                uint32_t sbv[T2_GU_BATCH][2];
+                bool lv[T2_GU_BATCH], hv[T2_GU_BATCH];
+                int is[T2_GU_BATCH], kes[T2_GU_BATCH];
 #pragma unroll
-                for (int v = 0; v < 2; ++v) {
+                for (int v = 0; v < T2_GU_BATCH; ++v) {
                     const int pr = pb + v * step + rm.r;
                     lv[v] = rm.active && pr < p1;
                     const int u = sp.u0 + pr / 32;
                     kes[v] = u / sp.HG;
                     is[v] = (u % sp.HG) * 32 + pr % 32;
-                    exs[v] = lv[v] ? slot_s[kes[v] < K ? kes[v] : K] : nullptr;
-                    if (exs[v]) {
-                        const uint8_t* gp = exs[v] + (size_t)is[v] * H + 32 * rm.g;
-                        c[v][0] = ldg_stream(gp);
-                        c[v][1] = ldg_stream(gp + 16);
-                        c[v][2] = ldg_stream(gp + H / 2);
-                        c[v][3] = ldg_stream(gp + H / 2 + 16);
-                        sbv[v][0] = ldg_u32(exs[v] + sl.gu_sb() + ((size_t)(2 * is[v]) * GH + rm.g) * 4);
-                        sbv[v][1] = ldg_u32(exs[v] + sl.gu_sb() + ((size_t)(2 * is[v] + 1) * GH + rm.g) * 4);
+                    hv[v] = false;
+                    if (lv[v]) {
+                        int sg = 0;
+                        while (sg < plan.n_gu && plan.gu_pos[sg + 1] <= pr) ++sg;
+                        const uint8_t* cb;
+                        const uint8_t* sbb;
+                        int rr;
+                        if (sg < plan.n_gu) {
+                            cb = plan.gu_codes(sg);
+                            sbb = plan.gu_sb(sg);
+                            rr = pr - plan.gu_pos[sg];
+                        } else {  // beyond the staged runs: the slot in global memory
+                            const uint8_t* ex = slot_s[kes[v] < K ? kes[v] : K];
+                            cb = ex;
+                            sbb = ex ? ex + sl.gu_sb() : nullptr;
+                            rr = is[v];
+                        }
+                        if (cb && sbb) {
+                            const uint8_t* gp = cb + (size_t)rr * H + 32 * rm.g;
+                            c[v][0] = *reinterpret_cast<const uint4*>(gp);
+                            c[v][1] = *reinterpret_cast<const uint4*>(gp + 16);
+                            c[v][2] = *reinterpret_cast<const uint4*>(gp + H / 2);
+                            c[v][3] = *reinterpret_cast<const uint4*>(gp + H / 2 + 16);
+                            const uint8_t* sp2 = sbb + (size_t)rr * 2 * GH * 4 + rm.g * 4;
+                            sbv[v][0] = *reinterpret_cast<const uint32_t*>(sp2);
+                            sbv[v][1] = *reinterpret_cast<const uint32_t*>(sp2 + GH * 4);
+                            hv[v] = true;
+                        }
                     }
                 }
 #pragma unroll
-                for (int v = 0; v < 2; ++v) {
+                for (int v = 0; v < T2_GU_BATCH; ++v) {
                     const int pr = pb + v * step + rm.r;
                     float pg = 0.f, pu = 0.f;
-                    if (exs[v]) {
+                    if (hv[v]) {
                         pg = q4_group_dot(c[v][0], c[v][1], hpl + rm.g, hxg[rm.g], sbv[v][0], GH);
                         pu = q4_group_dot(c[v][2], c[v][3], hpl + rm.g, hxg[rm.g], sbv[v][1], GH);
                     }
@@ -501,12 +962,14 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                     pu = seg_sum(pu, rm.G, lane);
                     const int lead = lane - rm.g;
                     float a = 0.f;
-                    if (lv[v] && rm.g == 0 && exs[v]) {
+                    if (lv[v] && rm.g == 0 && hv[v]) {
                         if (kes[v] == K && lora) {
                             float dg = 0.f, du = 0.f;
+                            const __half* bgr = plan.bg() ? plan.bg() + (size_t)(pr - ps_m) * rank : L.Bg + (size_t)is[v] * rank;
+                            const __half* bur = plan.bu() ? plan.bu() + (size_t)(pr - ps_m) * rank : L.Bu + (size_t)is[v] * rank;
                             for (int rr = 0; rr < rank; ++rr) {
-                                dg = fmaf(__half2float(L.Bg[(size_t)is[v] * rank + rr]), zg[rr], dg);
-                                du = fmaf(__half2float(L.Bu[(size_t)is[v] * rank + rr]), zu[rr], du);
+                                dg = fmaf(__half2float(bgr[rr]), zg[rr], dg);
+                                du = fmaf(__half2float(bur[rr]), zu[rr], du);
                             }
                             pg = fmaf(L.lscale, dg, pg);
                             pu = fmaf(L.lscale, du, pu);
@@ -520,126 +983,137 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                         for (int m = rm.G; m < TEAM; ++m) cl_st(cl_map(ateam + pr, m), av);
                 }
             }
-        }
-
-        // ---- the next layer's weights start moving into L2 now (this CTA's share)
-        if (l + 1 < Lz) {
-            const LayerP N = S.layers[l + 1];
-            if (!layer_native(S, N, t)) {
-                for (int k = 0; k < K; ++k) prefetch_share_lines(slot_all[(l + 1) * (K + 1) + k], sbytes, b, nb);
-            } else if (N.W_r) {
-                prefetch_share_lines(N.W_r, (size_t)E * H * 2, b, nb);
-            }
-            if (N.sh) prefetch_share_lines(N.sh, sbytes, b, nb);
-            if (N.fc1) {
-                prefetch_share_lines(N.fc1, (size_t)N.hidden * (H + 2 * E) * 2, b, nb);
-                prefetch_share_lines(N.lres, (size_t)E * (H + 2 * E) * 2, b, nb);
-            }
-            if (L.fc1) prefetch_share_lines(L.fc2, (size_t)E * L.hidden * 2, b, nb);
-        }
-
-        // ---- team exchange of the activations
-        cl_sync();
-
-        // quantise the team's activations (one half-group per warp) and the
-        // LoRA B input zd = A_down[:, team cols] . a_s of the shared rows
-        const int nu = sp.u1 - sp.u0;
-        for (int u = warp; u < nu; u += NW) quantize_half_warp(ateam[u * 32 + lane], apl + u * 4, axg + u, lane);
-        if (team_lora) {
-            const int us0 = max(sp.u0, K * sp.HG);
-            for (int rr = warp; rr < rank; rr += NW) {
-                float acc = 0.f;
-                for (int p = (us0 - sp.u0) * 32 + lane; p < sp.rows; p += 32) {
-                    const int i = ((sp.u0 + p / 32) % sp.HG) * 32 + p % 32;
-                    acc = fmaf(__half2float(L.Ad[(size_t)rr * I + i]), ateam[p], acc);
+            // this CTA's gate/up side has been read: the issuing head warp may
+            // bring in the next layer's
+            asm volatile("bar.arrive 2, %0;" ::"r"(T2_EXPERT_W * 32 + 32));
+            // ---- team exchange of the activations
+            cl_sync();
+            if (!mbar_wait2(&sbar[1 + (l & 1)], (l >> 1) & 1)) set_status(st, E0_ST_TIMEOUT);
+            // quantise the team's activations (one half-group per warp) and the
+            // LoRA B input zd = A_down[:, team cols] . a_s of the shared rows
+            const int nu = sp.u1 - sp.u0;
+            for (int u = warp; u < nu; u += T2_EXPERT_W) quantize_half_warp(ateam[u * 32 + lane], apl + u * 4, axg + u, lane);
+            if (team_lora) {
+                const int us0 = max(sp.u0, K * sp.HG);
+                for (int rr = warp; rr < rank; rr += T2_EXPERT_W) {
+                    float acc = 0.f;
+                    const int i0t = (us0 - K * sp.HG) * 32;  // the team's first shared column
+                    for (int p = (us0 - sp.u0) * 32 + lane; p < sp.rows; p += 32) {
+                        const int i = ((sp.u0 + p / 32) % sp.HG) * 32 + p % 32;
+                        const float ad = plan.ad(db, 0) ? __half2float(plan.ad(db, rr)[i - i0t])
+                                                        : __half2float(L.Ad[(size_t)rr * I + i]);
+                        acc = fmaf(ad, ateam[p], acc);
+                    }
+                    acc = warp_sum(acc);
+                    if (lane == 0) zd[rr] = acc;
                 }
-                acc = warp_sum(acc);
-                if (lane == 0) zd[rr] = acc;
             }
-        }
-        __syncthreads();
-
-        const int rows_m = H / TEAM;              // output rows of this member
-        const int ndw = (rows_m + 31) / 32;       // warps on the down rows
-        if (warp < ndw) {
+            asm volatile("bar.sync 1, %0;" ::"r"(T2_EXPERT_W * 32));
             // ---- down rows: lane = output row, partial over the team's columns
-            const int j = crank * rows_m + warp * 32 + lane;
-            const bool live = warp * 32 + lane < rows_m;
-            float acc = 0.f;
-            for (int ub = sp.u0; ub < sp.u1; ub += 8) {
-                uint4 cv[8];
-                uint32_t sbv[8];
+            for (int jr = warp * 32 + lane; jr - lane < rows_m; jr += T2_EXPERT_W * 32) {
+                if (jr >= rows_m) continue;
+                const int j = j0 + jr;
+                float acc = 0.f;
+                for (int ub = sp.u0; ub < sp.u1; ub += 8) {
+                    uint4 cv[8];
+                    uint32_t sbv[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int u = ub + q;
-                    const uint8_t* ex = (live && u < sp.u1) ? slot_s[u / sp.HG < K ? u / sp.HG : K] : nullptr;
-                    if (ex) {
-                        const int hg = u % sp.HG;
-                        cv[q] = ldg_stream(ex + sl.down_codes() + ((size_t)hg * H + j) * 16);
-                        sbv[q] = ldg_u32(ex + sl.down_sb() + ((size_t)(hg / 2) * H + j) * 4);
+                    for (int q = 0; q < 8; ++q) {
+                        const int u = ub + q;
+                        if (u < sp.u1 && plan.dn_codes(db, u - sp.u0) && plan.dn_sb(db, u - sp.u0)) {
+                            cv[q] = *reinterpret_cast<const uint4*>(plan.dn_codes(db, u - sp.u0) + (size_t)jr * 16);
+                            sbv[q] = *reinterpret_cast<const uint32_t*>(plan.dn_sb(db, u - sp.u0) + (size_t)jr * 4);
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int u = ub + q;
+                        if (u >= sp.u1 || !plan.dn_codes(db, u - sp.u0) || !plan.dn_sb(db, u - sp.u0)) continue;
+                        const int ke = u / sp.HG;
+                        const float d = q4_half_dot(cv[q], apl + (u - sp.u0) * 4, axg[u - sp.u0], sbv[q]);
+                        acc = fmaf(ke < K ? w_s[ke] : 1.f, d, acc);
                     }
                 }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int u = ub + q;
-                    if (!live || u >= sp.u1) continue;
-                    const int ke = u / sp.HG;
-                    if (!slot_s[ke < K ? ke : K]) continue;
-                    const float d = q4_half_dot(cv[q], apl + (u - sp.u0) * 4, axg[u - sp.u0], sbv[q]);
-                    acc = fmaf(ke < K ? w_s[ke] : 1.f, d, acc);
+                if (team_lora) {
+                    float d = 0.f;
+                    const __half* bdr = plan.bd(db) ? plan.bd(db) + (size_t)jr * rank : L.Bd + (size_t)j * rank;
+                    for (int rr = 0; rr < rank; ++rr) d = fmaf(__half2float(bdr[rr]), zd[rr], d);
+                    acc = fmaf(L.lscale, d, acc);
                 }
+                if (nu > 0)
+                    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(S.y_acc + (size_t)(l % 3) * H + j), "f"(acc)
+                                 : "memory");
             }
-            if (team_lora && live) {
-                float d = 0.f;
-                for (int rr = 0; rr < rank; ++rr) d = fmaf(__half2float(L.Bd[(size_t)j * rank + rr]), zd[rr], d);
-                acc = fmaf(L.lscale, d, acc);
-            }
-            if (live && nu > 0)
-                asm volatile("red.global.add.f32 [%0], %1;" ::"l"(S.y_acc + (size_t)(l % 3) * H + j), "f"(acc)
-                             : "memory");
         } else {
-            // ---- prerouter heads on the remaining warps: routing of owner
-            // l-2's logits, fc2 of owner l-1, fc1 and the linear residual of owner l
-            const int hw = NW - ndw;
-            const int aw = b * hw + (warp - ndw), naw = nb * hw;
-            if (b == 0 && warp == ndw && l >= 2 && S.layers[l - 2].fc1)
+            // ---- head warps: nothing they do feeds the team exchange, so they
+            // arrive at it now and wait at the end of the layer
+            cl_arrive();
+            // the next layer's down side goes to the other down region now
+            if (warp == HW && next_known) stage_dn_for(l + 1);
+            // one warp of the last block (not the issuing one) routes owner l-2's logits
+            if (b == nb - 1 && warp == HW + 1 && l >= 2 && lyr[l - 2].fc1)
                 stack_route_head(S, l - 2, t, scr, tr, st, lane, S.z2 + (size_t)((l - 1) & 1) * E);
-            const LayerP P = l >= 1 ? S.layers[l - 1] : L;
+        }
+
+        // ---- prerouter heads: fc2 of owner l-1 (four rows a unit) and fc1 /
+        // linear residual of owner l (one row a unit).  This block's units are
+        // handed out one at a time: the head warps start right away, the expert
+        // warps join once their down rows are done.
+        {
+            const LayerP& P = l >= 1 ? lyr[l - 1] : L;
             const int hidP = (l >= 1 && P.fc1) ? P.hidden : 0;
             const int n_fc2 = hidP > 0 ? E : 0;
             const int n_fc1 = L.fc1 ? L.hidden : 0;
-            const int n_lres = L.fc1 ? E : 0;
+            const int n_row = L.fc1 ? L.hidden + E : 0;  // fc1 rows, then linear-residual rows
+            const int nA = (n_fc2 + 3) / 4;
+            const int u_hi = (int)((long)(b + 1) * (nA + n_row) / nb);
             const int32_t* prev = t > 0 ? S.hist + ((size_t)((t + 1) & 1) * Lz + l) * K : nullptr;
-            for (int it = aw; it < n_fc2 + n_fc1 + n_lres; it += naw) {
-                if (it < n_fc2) {
-                    const int e = it;
-                    const float acc = warp_sum(
-                        hrow_dot_gelu(P.fc2 + (size_t)e * hidP, S.hpre2 + (size_t)((l - 1) & 1) * hidP, hidP, lane));
-                    if (lane == 0)
-                        S.z2[(size_t)(l & 1) * E + e] = acc + (P.b2 ? __half2float(P.b2[e]) : 0.f) +
-                                                        __ldcg(S.zres2 + (size_t)((l - 1) & 1) * E + e);
+            while (true) {
+                int it = 0;
+                if (lane == 0) it = atomicAdd(hnext, 1);
+                it = __shfl_sync(0xffffffffu, it, 0);
+                if (it >= u_hi) break;
+                if (it < nA) {
+                    const int e0 = 4 * it, nr = min(4, n_fc2 - e0);
+                    float acc[4];
+                    hrow_dot_gelu4(P.fc2 + (size_t)e0 * hidP, (size_t)hidP, nr, S.hpre2 + (size_t)((l - 1) & 1) * hidP,
+                                   hidP, lane, acc);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float v = warp_sum(acc[q]);
+                        if (lane == 0 && q < nr)
+                            S.z2[(size_t)(l & 1) * E + e0 + q] = v + (P.b2 ? __half2float(P.b2[e0 + q]) : 0.f) +
+                                                                 __ldcg(S.zres2 + (size_t)((l - 1) & 1) * E + e0 + q);
+                    }
                 } else {
-                    const int q = it - n_fc2;
-                    const bool is_fc1 = q < n_fc1;
-                    const int row = is_fc1 ? q : q - n_fc1;
-                    const __half* wr = (is_fc1 ? L.fc1 : L.lres) + (size_t)row * ((size_t)H + 2 * E);
-                    float acc = hrow_dot(wr, h, H, lane);
+                    const int q = it - nA;
+                    const __half* wr = q < n_fc1 ? L.fc1 + (size_t)q * ((size_t)H + 2 * E)
+                                                 : L.lres + (size_t)(q - n_fc1) * ((size_t)H + 2 * E);
+                    float a0 = hrow_dot(wr, h, H, lane);
                     // the one-hot columns: this layer's experts, then the previous token's
                     if (lane < 2 * K) {
                         const int e = lane < K ? inds_s[lane] : (prev ? __ldcg(prev + lane - K) : -1);
-                        if (e >= 0 && e < E) acc += __half2float(wr[(lane < K ? (size_t)H : (size_t)H + E) + e]);
+                        if (e >= 0 && e < E) a0 += __half2float(wr[(lane < K ? (size_t)H : (size_t)H + E) + e]);
                     }
-                    acc = warp_sum(acc);
+                    a0 = warp_sum(a0);
                     if (lane == 0) {
-                        if (is_fc1)
-                            S.hpre2[(size_t)(l & 1) * L.hidden + row] = acc + (L.b1 ? __half2float(L.b1[row]) : 0.f);
+                        if (q < n_fc1)
+                            S.hpre2[(size_t)(l & 1) * L.hidden + q] = a0 + (L.b1 ? __half2float(L.b1[q]) : 0.f);
                         else
-                            S.zres2[(size_t)(l & 1) * E + row] = acc;
+                            S.zres2[(size_t)(l & 1) * E + (q - n_fc1)] = a0;
                     }
                 }
             }
         }
-        grid_barrier2(Sp, bar0 + (unsigned long long)(++nbar) * nb, st);
+        if (warp >= T2_EXPERT_W) {
+            if (warp == HW) {
+                // wait until this CTA's gate/up side has been read, then bring in the next layer's
+                asm volatile("bar.sync 2, %0;" ::"r"(T2_EXPERT_W * 32 + 32));
+                if (next_known) stage_gu_for(l + 1);
+            }
+            cl_wait();
+        }
+        grid_barrier_team(Sp, bar0 + (unsigned long long)(++nbar) * NT, st);
     }
 
     // ---- token output, the last pending prediction, bookkeeping
@@ -650,14 +1124,14 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             r_out[j] = v;
             if (tr.r) tr.r[(size_t)Lz * H + j] = v;
         }
-        if (warp == 1 && Lz >= 2 && S.layers[Lz - 2].fc1)
+        if (warp == 1 && Lz >= 2 && lyr[Lz - 2].fc1)
             stack_route_head(S, Lz - 2, t, scr, tr, st, lane, S.z2 + (size_t)((Lz - 1) & 1) * E);
         __syncthreads();
         // layer 0 of the next token accumulates into buffer 0
         for (int j = tid; j < H; j += T2_THREADS) S.y_acc[j] = 0.f;
         if (tid == 0) {
-            S.t = t + 1;
-            S.bar_base = bar0 + (unsigned long long)nbar * nb;
+            Sp->t = t + 1;
+            Sp->bar_base = bar0 + (unsigned long long)nbar * NT;
         }
     }
 }
