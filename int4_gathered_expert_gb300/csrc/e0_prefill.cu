@@ -556,29 +556,43 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 if (MODE == MODE_GATEUP) sbp = ex + sl.gu_sb() + (size_t)wr * (p.H / GROUP) * 4;
                 else sbp = ex + sl.down_sb() + (size_t)wr * 4;  // group kk at + kk * H * 4
             }
-            for (int kk = 0; kk < nk; ++kk, ++g) {
-                const uint32_t s = g % P2_STAGES;
-                const uint32_t sbits =
-                    ex ? ldg_u32(sbp + (MODE == MODE_GATEUP ? (size_t)kk * 4 : (size_t)kk * p.H * 4)) : 0u;
-                if (!mbar_wait(&raw_full[s], (g / P2_STAGES) & 1, abort, WAIT_LIMIT_NS)) {
-                    ok = false;
-                    *abort = 1;
-                    atomicOr(p.err, 16u);
-                    break;
+            // (scale, bias) words of 8 K steps are loaded one chunk ahead of use
+            const size_t sstep = MODE == MODE_GATEUP ? (size_t)4 : (size_t)p.H * 4;
+            uint32_t sbw[8], sbn[8];
+#pragma unroll
+            for (int d = 0; d < 8; ++d) sbn[d] = (ex && d < nk) ? ldg_u32(sbp + (size_t)d * sstep) : 0u;
+            for (int k0 = 0; k0 < nk && ok; k0 += 8) {
+#pragma unroll
+                for (int d = 0; d < 8; ++d) {
+                    sbw[d] = sbn[d];
+                    sbn[d] = (ex && k0 + 8 + d < nk) ? ldg_u32(sbp + (size_t)(k0 + 8 + d) * sstep) : 0u;
                 }
-                uint8_t* st = smem + s * P2_STAGE;
-                if (ex) {
-                    // gate/up raw tile: [128 rows][32 B]; down raw tile: [2 half-groups][128 rows][16 B]
-                    const uint8_t* raw = st + P2_A + P2_B;
-                    const uint4 c0 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 : raw + r * 16);
-                    const uint4 c1 =
-                        *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 + 16 : raw + 2048 + r * 16);
-                    dequant64_to_tile(c0, c1, sbits, st, r);
-                } else {
-                    zero_row_of_tile(st, r);
+#pragma unroll
+                for (int d = 0; d < 8; ++d) {
+                    const int kk = k0 + d;
+                    if (kk >= nk) break;
+                    const uint32_t s = g % P2_STAGES;
+                    if (!mbar_wait(&raw_full[s], (g / P2_STAGES) & 1, abort, WAIT_LIMIT_NS)) {
+                        ok = false;
+                        *abort = 1;
+                        atomicOr(p.err, 16u);
+                        break;
+                    }
+                    uint8_t* st = smem + s * P2_STAGE;
+                    if (ex) {
+                        // gate/up raw tile: [128 rows][32 B]; down raw tile: [2 half-groups][128 rows][16 B]
+                        const uint8_t* raw = st + P2_A + P2_B;
+                        const uint4 c0 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 : raw + r * 16);
+                        const uint4 c1 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 + 16
+                                                                                              : raw + 2048 + r * 16);
+                        dequant64_to_tile(c0, c1, sbw[d], st, r);
+                    } else {
+                        zero_row_of_tile(st, r);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&a_full[s]);
+                    ++g;
                 }
-                fence_proxy_async_smem();
-                mbar_arrive(&a_full[s]);
             }
         }
     } else if (warp < 8) {
