@@ -50,27 +50,35 @@ def parse():
     p.add_argument("--layers", type=int, default=40, help="fewer layers: a small case for profiling only")
     p.add_argument("--no-prefill", action="store_true", help="skip the whole-layer prefill measurement")
     p.add_argument("--prefill-only", action="store_true")
+    p.add_argument("--route-k", type=int, default=4, help="routed experts per token (the 35B tier uses 4)")
+    p.add_argument("--no-prerouter", action="store_true",
+                   help="every layer routes with its own router; no prerouter heads")
     return p.parse_args()
 
 
 # ---------------------------------------------------------------- prefill (T=4096 whole-layer)
 
 
-def run_prefill_bench(dev, reps: int = 5):
-    """Whole-layer prefill of the 35B-tier layer, T=4096, Zipf(1.1) expert
-    load; the L2 is flushed (a 256 MB write) before every timed call."""
+def run_prefill_bench(dev, reps: int = 5, tier: str = "35b"):
+    """Whole-layer prefill, T=4096: the 35B-tier layer with a Zipf(1.1) expert
+    load (softmax-top-4), or the 8B-tier layer (sigmoid-group, K=8); the L2 is
+    flushed (a 256 MB write) before every timed call."""
     import torch
     from int4_gathered_expert_gb300 import lib as L
     from int4_gathered_expert_gb300 import synth
     from int4_gathered_expert_gb300.model import SlotPoolDev
-    d = synth.prefill35b(4, T=4096)
+    d = synth.prefill35b(4, T=4096) if tier == "35b" else synth.prefill8b(5, T=4096)
     s = d["shape"]
     T = d["X"].shape[0]
     pool = SlotPoolDev.resident(d["bank"], s.H, s.I)
     X = torch.from_numpy(d["X"]).to(dev)
     Wr = torch.from_numpy(d["router"]).to(dev)
-    bias = torch.from_numpy(d["logit_bias"]).to(dev)
-    rp = L.route_params(K=s.K, logit_bias=bias)
+    if tier == "35b":
+        bias = torch.from_numpy(d["logit_bias"]).to(dev)
+        rp = L.route_params(K=s.K, logit_bias=bias)
+    else:
+        rp = L.route_params(mode=L.E0_ROUTE_SIGMOID_GROUP, K=s.K, n_groups=s.n_groups, topk_groups=s.topk_groups,
+                            scale=s.route_scale)
     ws_bytes = L.e0_workspace_size(2, T, s.H, s.I, s.E, s.K)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     Y = torch.empty((T, s.H), dtype=torch.float32, device=dev)
@@ -95,7 +103,9 @@ def run_prefill_bench(dev, reps: int = 5):
     flops = 2.0 * T * s.K * 3 * s.H * s.I
     pk = peaks()
     peak = pk["bf16_tflops"] if pk else 1900.0
-    return {"workload": "35B-tier whole-layer prefill, T=4096, K=4, Zipf(1.1) expert load",
+    name = ("35B-tier whole-layer prefill, T=4096, K=4, Zipf(1.1) expert load" if tier == "35b" else
+            "8B-tier whole-layer prefill, T=4096, H=1536, I=384, E=128, sigmoid-group n=8 G=4 K=8")
+    return {"workload": name,
             "value": T / t, "unit": "tok/s", "ms": t * 1e3, "useful_tflops": flops / t / 1e12,
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peak, "unit": "TFLOP/s",
                          "frac": flops / t / 1e12 / peak, "traffic": None,
@@ -314,13 +324,18 @@ def run_gb300(args):
     from int4_gathered_expert_gb300.model import StackDev
 
     if args.prefill_only:
-        print(json.dumps({"prefill": run_prefill_bench(dev)}), flush=True)
+        print(json.dumps({"prefill": run_prefill_bench(dev), "prefill_8b": run_prefill_bench(dev, tier="8b")}),
+              flush=True)
         return 0
     shape = synth.STACK35B
+    import dataclasses
     if args.layers != shape.n_layers:
-        import dataclasses
         shape = dataclasses.replace(shape, n_layers=args.layers,
                                     owners=tuple(o for o in shape.owners if o + 1 < args.layers))
+    if args.route_k != shape.layer.K:
+        shape = dataclasses.replace(shape, layer=dataclasses.replace(shape.layer, K=args.route_k))
+    if args.no_prerouter:
+        shape = dataclasses.replace(shape, owners=())
     tps = args.tokens_per_step
     n_tok = (args.warmup + args.steps) * tps
     model = synth.stack_model(shape, n_tokens=n_tok)
@@ -411,18 +426,23 @@ def run_gb300(args):
                "sample": f"first {n_cpu} tokens of the same stream (token 0 routes all 40 layers natively) "
                          "through the 40-layer stack, float64 numpy oracle"}
 
-    prefill = None
+    prefill = prefill8 = None
     if rank == 0 and not args.no_prefill:
         del sd
         torch.cuda.empty_cache()
         prefill = run_prefill_bench(dev)
+        torch.cuda.empty_cache()
+        prefill8 = run_prefill_bench(dev, tier="8b")
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "int4 x int16 dp4a -> int32, f32 epilogue",
                 "data": "synthetic",
-                "config": {"workload": WORKLOAD, "tokens_per_step": tps, "batch": 1,
+                "config": {"workload": WORKLOAD if (args.route_k == 4 and not args.no_prerouter and args.layers == 40)
+                           else WORKLOAD + " [variant: K=%d, prerouter %s, %d layers]" % (
+                               args.route_k, "off" if args.no_prerouter else "on", args.layers),
+                           "tokens_per_step": tps, "batch": 1,
                            "l2": "no flush: each token streams %.0f MB of weights, more than the 129 MB L2"
                                  % (nb["total"] / 1e6),
                            "kernel": {0: "persistent cooperative kernel, one launch per token",
@@ -435,7 +455,7 @@ def run_gb300(args):
                              "frac": achieved / peak, "traffic": traffic,
                              "kernel": kname, "launch_us": mean_launch_s * 1e6,
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback"},
-                "cpu_baseline": cpu, "e2e": e2e, "prefill": prefill, "gpu_launches": n_timed * LAUNCHES_PER_TOKEN.get(args.kernel_impl, 6 * shape.n_layers + 1),
+                "cpu_baseline": cpu, "e2e": e2e, "prefill": prefill, "prefill_8b": prefill8, "gpu_launches": n_timed * LAUNCHES_PER_TOKEN.get(args.kernel_impl, 6 * shape.n_layers + 1),
                 "clocks": clocks, "device_status": st}
         print(json.dumps(line), flush=True)
     if ws > 1:

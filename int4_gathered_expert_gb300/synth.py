@@ -284,6 +284,16 @@ def prefill35b(seed: int = 4, T: int = 4096) -> dict:
             "X": normal_rows(seed, T, s.H).astype(np.float16)}
 
 
+def prefill8b(seed: int = 5, T: int = 4096) -> dict:
+    """8B-tier whole-layer prefill: X fp16 [T, H] ~ N(0,1), router N(0, 1/sqrt(H))
+    so the logits are ~N(0,1), sigmoid-group routing (n=8, G=4, s=2.5, K=8),
+    no logit skew."""
+    s = L8B
+    return {"shape": s, "bank": expert_bank(seed, 0, s, threads=3),
+            "router": router(seed, 0, s, std=1.0 / np.sqrt(s.H)),
+            "X": normal_rows(seed, T, s.H).astype(np.float16)}
+
+
 def expert_nbytes(shape: LayerShape) -> int:
     """Bytes of one expert in the canonical format (codes + fp16 scale + fp16 bias)."""
     H, I = shape.H, shape.I

@@ -126,3 +126,37 @@ def test_35b_prefill_full_size(L, prefill35):
     Yo = O.moe_block(d["X"][sample].astype(np.float64), O.BankExperts(d["bank"]), rt.inds[sample], rt.w[sample])
     errs = [rel_l2(Y[t], Yo[i]) for i, t in enumerate(sample)]
     assert max(errs) <= REL_L2, max(errs)
+
+
+@pytest.fixture(scope="module")
+def prefill8(L):
+    from int4_gathered_expert_gb300.model import SlotPoolDev
+    d = synth.prefill8b(5, T=3100)
+    s = d["shape"]
+    d["pool"] = SlotPoolDev.resident(d["bank"], s.H, s.I)
+    return d
+
+
+def test_8b_prefill_sigmoid_group(L, prefill8):
+    """The 8B-tier layer (H=1536, I=384, E=128) through the same sorted grouped
+    GEMMs, with sigmoid-group routing (n=8, keep 4 groups, K=8, s=2.5) over a
+    3.1k-token prompt: every token's routing against the oracle (exact up to
+    the tie rule) and outputs on a sample of tokens."""
+    d = prefill8
+    s = d["shape"]
+    T = d["X"].shape[0]
+    rp = L.route_params(mode=L.E0_ROUTE_SIGMOID_GROUP, K=s.K, n_groups=s.n_groups, topk_groups=s.topk_groups,
+                        scale=s.route_scale)
+    Y, inds, w, st = run_prefill(L, d["pool"], dev(d["X"]), dev(d["router"]), rp, T)
+    assert st == 0
+    logits = O.router_logits(d["router"], d["X"])
+    rt = O.route(logits, s)
+    ex, msgs = routing_matches(inds, w, rt)
+    assert not msgs, msgs[:4]
+    counts = np.bincount(inds.ravel(), minlength=s.E)
+    assert counts.sum() == T * s.K
+    g = np.random.default_rng(1)
+    sample = sorted(set([0, T - 1] + g.choice(T, 22, replace=False).tolist()) - set(ex))
+    Yo = O.moe_block(d["X"][sample].astype(np.float64), O.BankExperts(d["bank"]), rt.inds[sample], rt.w[sample])
+    errs = [rel_l2(Y[t], Yo[i]) for i, t in enumerate(sample)]
+    assert max(errs) <= REL_L2, max(errs)
