@@ -295,7 +295,11 @@ typedef struct e0_stack_trace {
 size_t e0_stack_workspace_size(int L, int H, int I, int E, int K, int head_hidden);
 
 /* Copy the layer descriptors into the workspace and clear the routing
- * history (the next step is token 0).  Synchronises the stream. */
+ * history (the next step is token 0).  Synchronises the stream.  Also sizes
+ * the cluster kernel (impl 2): its teams and the shared-memory regions that
+ * hold each layer's weight slices; slices that do not fit are read from
+ * global memory.  The environment variable E0MOE_STAGE_LIMIT (bytes), when
+ * set, lowers that shared-memory budget (a test hook for the global path). */
 int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
                      const e0_route_params* rp, void* ws, size_t ws_bytes, e0_stream_t stream);
 

@@ -2,6 +2,7 @@
 // points for packing, slot update, routing, RMSNorm, the MoE block, the
 // prerouter head and the whole-token decode stack.
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <map>
@@ -890,7 +891,14 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
         // teams: as many 8-CTA clusters as can be resident at once with the
         // largest shared-memory footprint; every team must hold at most
         // T2_MAX_UNITS half-groups of a layer
-        const size_t limit = smem_optin();
+        size_t limit = smem_optin();
+        // E0MOE_STAGE_LIMIT (bytes) caps the block's shared memory, so that the
+        // weight slices that no longer fit are read from global memory (a test
+        // hook for that path)
+        if (const char* env = getenv("E0MOE_STAGE_LIMIT")) {
+            const long v = atol(env);
+            if (v > 0 && (size_t)v < limit) limit = (size_t)v;
+        }
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3((num_sms() / TEAM) * TEAM);

@@ -152,3 +152,21 @@ def test_tiny_stack_cluster_kernel(L):
     traces = run_stack(sd, m, 4, impl=2)
     assert L.e0_read_status(sd.status) == 0
     check_stack(m, traces, (0, 1, 2, 3))
+
+
+@pytest.mark.parametrize("limit", [120000, 96000])
+def test_35b_cluster_kernel_partial_staging(L, stack35, limit, monkeypatch):
+    """With the shared-memory budget lowered, some (120 KB: the down slices) or
+    most (96 KB: part of the gate/up rows too) weight slices are read from
+    global memory instead of the staging regions; results must not change."""
+    m, sd = stack35
+    a = run_stack(sd, m, 3, impl=0)
+    monkeypatch.setenv("E0MOE_STAGE_LIMIT", str(limit))
+    b = run_stack(sd, m, 3, impl=2)
+    monkeypatch.delenv("E0MOE_STAGE_LIMIT")
+    sd.prepare()
+    assert L.e0_read_status(sd.status) == 0
+    for t in range(3):
+        assert rel_l2(b[t]["r"], a[t]["r"]) < 1e-4, t
+        same = (a[t]["inds"] == b[t]["inds"]).all(axis=1)
+        assert same.mean() > 0.95, (t, same.mean())
