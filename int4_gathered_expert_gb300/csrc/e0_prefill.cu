@@ -30,7 +30,7 @@ constexpr int STAGES = 4;
 constexpr float REFINE_GAP = 2e-4f;  // well above the error of fp32 tensor-core accumulation over K = H
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
-enum { MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
+enum { MODE_GATEUP = 1, MODE_DOWN = 2 };
 
 struct PrefillWs {
     float* logits;      // [T][E]
@@ -204,37 +204,25 @@ struct GemmP {
     uint32_t* st;
 };
 
-// One CTA computes one 128-row x BN-column output tile.  Roles:
-//   warps 0-3  (grouped modes) each thread dequantises one weight row of the
-//              A tile per K step into shared memory; afterwards all four warps
-//              drain the accumulator from TMEM (thread t owns TMEM lane t);
-//   warp 4     issues the TMA loads of the B tile (and of A for the router);
+// Router GEMM: logits[T][E] = X W_r^T on the tensor cores.  One CTA computes
+// one 128-row (experts) x BN-column (tokens) output tile.  Roles:
+//   warps 0-3  drain the accumulator from TMEM (thread t owns TMEM lane t);
+//   warp 4     issues the TMA loads of both operand tiles;
 //   warp 5     allocates TMEM and, from one thread, issues tcgen05.mma.
 // Pipeline: STAGES shared-memory stages guarded by full/empty mbarriers; the
 // MMA thread frees a stage with tcgen05.commit.  Every wait is time-bounded:
 // on timeout the CTA raises *err, stops its loops, frees TMEM and returns.
-template <int MODE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    k_umma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmP p) {
-    constexpr int NA = MODE == MODE_GATEUP ? 2 : 1;
+    k_router_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmP p) {
     constexpr uint32_t A_BYTES = BM * BK * 2;
     constexpr uint32_t B_BYTES = BN * BK * 2;
-    constexpr uint32_t STAGE_BYTES = NA * A_BYTES + B_BYTES;
-    constexpr uint32_t TMEM_COLS = NA * BN;
+    constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    constexpr uint32_t TMEM_COLS = BN;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM;
-    int expert = -1, row0, ncount;
-    if (MODE == MODE_ROUTER) {
-        row0 = blockIdx.y * BN;
-        ncount = min(BN, p.T - row0);
-    } else {
-        if ((int)blockIdx.y >= *p.n_tiles) return;
-        const int4 tl = p.tiles[blockIdx.y];
-        expert = tl.x;
-        row0 = tl.y;
-        ncount = tl.w;
-    }
+    const int row0 = blockIdx.y * BN;
+    const int ncount = min(BN, p.T - row0);
     if (ncount <= 0) return;
     const int n_mma = (ncount + 15) & ~15;
     const int nk = p.K / BK;
@@ -249,7 +237,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], MODE == MODE_ROUTER ? 1 : BM + 1);
+            mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(accum, 1);
@@ -262,89 +250,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const uint8_t* ex = nullptr;
-    if (MODE != MODE_ROUTER) {
-        int slot = -1;
-        if (expert >= 0) slot = p.table[expert];
-        if (slot >= 0 && slot < p.n_slots) ex = p.pool + (size_t)slot * p.slot_bytes;
-        else if (threadIdx.x == 0) set_status(p.st, E0_ST_SLOT_MISS);
-    }
-
     if (warp < 4) {
-        // ---------------- dequant producers (grouped modes)
-        if (MODE != MODE_ROUTER) {
-            const int r = threadIdx.x;
-            const int row = m0 + r;
-            const bool live = ex != nullptr && row < p.rows_out;
-            const SlotLayout sl{p.H, p.I};
-            const uint8_t* c_a;
-            const uint8_t* c_b = nullptr;
-            const uint8_t* sb_a;
-            const uint8_t* sb_b = nullptr;
-            if (MODE == MODE_GATEUP) {
-                const int GH = p.H / GROUP;
-                c_a = ex + (size_t)row * p.H;
-                c_b = c_a + p.H / 2;
-                sb_a = ex + sl.gu_sb() + (size_t)(2 * row) * GH * 4;
-                sb_b = sb_a + (size_t)GH * 4;
-            } else {
-                const int GI = p.I / GROUP;
-                c_a = ex + sl.down_codes() + (size_t)row * (p.I / 2);
-                sb_a = ex + sl.down_sb() + (size_t)row * GI * 4;
-            }
-            constexpr int D = 4;  // K steps of codes kept in flight per thread
-            uint4 ra0[D], ra1[D], rb0[D], rb1[D];
-            uint32_t sa[D], sbv[D];
-#pragma unroll
-            for (int d = 0; d < D; ++d) {
-                if (live && d < nk) {
-                    ra0[d] = ldg_stream(c_a + d * 32);
-                    ra1[d] = ldg_stream(c_a + d * 32 + 16);
-                    sa[d] = ldg_u32(sb_a + d * 4);
-                    if (MODE == MODE_GATEUP) {
-                        rb0[d] = ldg_stream(c_b + d * 32);
-                        rb1[d] = ldg_stream(c_b + d * 32 + 16);
-                        sbv[d] = ldg_u32(sb_b + d * 4);
-                    }
-                }
-            }
-            bool ok = true;
-            for (int kb = 0; kb < nk && ok; kb += D) {
-#pragma unroll
-                for (int d = 0; d < D; ++d) {
-                    const int kk = kb + d;
-                    if (kk >= nk || !ok) break;
-                    const int s = kk % STAGES;
-                    if (!mbar_wait(&empty[s], ((kk / STAGES) + 1) & 1, abort, WAIT_LIMIT_NS)) {
-                        ok = false;
-                        *abort = 1;
-                        atomicOr(p.err, 1u);
-                        break;
-                    }
-                    uint8_t* a0 = smem + s * STAGE_BYTES;
-                    if (live) {
-                        dequant64_to_tile(ra0[d], ra1[d], sa[d], a0, r);
-                        if (MODE == MODE_GATEUP) dequant64_to_tile(rb0[d], rb1[d], sbv[d], a0 + A_BYTES, r);
-                    } else {
-                        zero_row_of_tile(a0, r);
-                        if (MODE == MODE_GATEUP) zero_row_of_tile(a0 + A_BYTES, r);
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&full[s]);
-                    const int kn = kk + D;
-                    if (live && kn < nk) {
-                        ra0[d] = ldg_stream(c_a + kn * 32);
-                        ra1[d] = ldg_stream(c_a + kn * 32 + 16);
-                        sa[d] = ldg_u32(sb_a + kn * 4);
-                        if (MODE == MODE_GATEUP) {
-                            rb0[d] = ldg_stream(c_b + kn * 32);
-                            rb1[d] = ldg_stream(c_b + kn * 32 + 16);
-                            sbv[d] = ldg_u32(sb_b + kn * 4);
-                        }
-                    }
-                }
-            }
-        }
         // ---------------- epilogue: TMEM -> registers -> global
         const bool have = mbar_wait(accum, 0, abort, WAIT_LIMIT_NS);
         if (!have) {
@@ -358,38 +264,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int c0 = 0; c0 < n_mma && have; c0 += 16) {
             float acc[16];
             tmem_ld16(tbase + c0, acc);
-            if (MODE == MODE_GATEUP) {
-                float up[16];
-                tmem_ld16(tbase + BN + c0, up);
-                tmem_ld_wait();
+            tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = c0 + j;
-                    if (col < ncount && row < p.rows_out)
-                        p.abuf[(size_t)(row0 + col) * p.I + row] = __float2half_rn(silu_f(acc[j]) * up[j]);
-                }
-            } else if (MODE == MODE_DOWN) {
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = c0 + j;
-                    if (col < ncount && row < p.rows_out)
-                        p.yp[(size_t)(row0 + col) * p.H + row] = p.wp[row0 + col] * acc[j];
-                }
-            } else {
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = c0 + j;
-                    if (col < ncount && row < p.rows_out) p.logits[(size_t)(row0 + col) * p.E + row] = acc[j];
-                }
+            for (int j = 0; j < 16; ++j) {
+                const int col = c0 + j;
+                if (col < ncount && row < p.rows_out) p.logits[(size_t)(row0 + col) * p.E + row] = acc[j];
             }
         }
     } else if (warp == 4) {
         // ---------------- TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tmB);
-            if (MODE == MODE_ROUTER) tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmA);
             for (int kk = 0; kk < nk; ++kk) {
                 const int s = kk % STAGES;
                 if (!mbar_wait(&empty[s], ((kk / STAGES) + 1) & 1, abort, WAIT_LIMIT_NS)) {
@@ -398,9 +284,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     break;
                 }
                 uint8_t* st = smem + s * STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[s], B_BYTES + (MODE == MODE_ROUTER ? A_BYTES : 0u));
-                tma_load_2d(&tmB, &full[s], st + NA * A_BYTES, kk * BK, row0);
-                if (MODE == MODE_ROUTER) tma_load_2d(&tmA, &full[s], st, kk * BK, m0);
+                mbar_arrive_expect_tx(&full[s], B_BYTES + A_BYTES);
+                tma_load_2d(&tmB, &full[s], st + A_BYTES, kk * BK, row0);
+                tma_load_2d(&tmA, &full[s], st, kk * BK, m0);
             }
         }
     } else {
@@ -418,14 +304,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
-                const uint32_t b_addr = a_addr + NA * A_BYTES;
+                const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
-                for (int j = 0; j < BK / 16; ++j) {
-                    const uint64_t bd = sdesc_k_sw128(b_addr + j * 32);
-                    umma_f16(tmem, sdesc_k_sw128(a_addr + j * 32), bd, idesc, (kk | j) != 0);
-                    if (MODE == MODE_GATEUP)
-                        umma_f16(tmem + BN, sdesc_k_sw128(a_addr + A_BYTES + j * 32), bd, idesc, (kk | j) != 0);
-                }
+                for (int j = 0; j < BK / 16; ++j)
+                    umma_f16(tmem, sdesc_k_sw128(a_addr + j * 32), sdesc_k_sw128(b_addr + j * 32), idesc, (kk | j) != 0);
                 umma_commit(&empty[s]);
             }
             if (ok) umma_commit(accum);
@@ -444,11 +326,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
 }
 
-template <int MODE>
-static size_t gemm_smem() {
-    constexpr int NA = MODE == MODE_GATEUP ? 2 : 1;
-    return (size_t)STAGES * (NA * BM * BK * 2 + BN * BK * 2) + 1024 + 256;
-}
+static size_t router_gemm_smem() { return (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256; }
 
 // ------------------------------------------------------------------ persistent grouped GEMM with TMA-fed dequant
 
@@ -938,8 +816,7 @@ static bool make_down_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t
 
 static std::once_flag g_prefill_init;
 static void prefill_attrs() {
-    cudaFuncSetAttribute(k_umma<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)gemm_smem<MODE_ROUTER>());
+    cudaFuncSetAttribute(k_router_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)router_gemm_smem());
     cudaFuncSetAttribute(k_umma2<MODE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm2_smem());
     cudaFuncSetAttribute(k_umma2<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm2_smem());
 }
@@ -992,7 +869,7 @@ int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, con
     // 1. router logits
     gp.K = H;
     gp.rows_out = E;
-    k_umma<MODE_ROUTER><<<dim3((E + BM - 1) / BM, (T + BN - 1) / BN), GEMM_THREADS, gemm_smem<MODE_ROUTER>(), s>>>(
+    k_router_gemm<<<dim3((E + BM - 1) / BM, (T + BN - 1) / BN), GEMM_THREADS, router_gemm_smem(), s>>>(
         mWr, mX, gp);
     // 2. routing (+ refinement of near-ties)
     int32_t* flag = w.flag;

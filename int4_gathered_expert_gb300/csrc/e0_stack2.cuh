@@ -3,25 +3,29 @@
 // The launch is made of teams: thread-block clusters of TEAM CTAs (one CTA
 // per SM).  Each layer's expert work — the K routed experts plus the shared
 // expert — is cut into half-groups of 32 intermediate rows; every team takes
-// a contiguous run of half-groups.  Inside a team each CTA computes a slice
-// of the SwiGLU activations a = silu(G h) * (U h) for the team's rows and
-// writes them into every team member's shared memory (distributed shared
-// memory), one cluster barrier later every member holds the team's
-// activations, quantises them, and computes the partial down projection
-// sum_k w_k D_k[:, team columns] a_k for its share of the output rows.  The
-// partial sums are added into the layer output y with red.add; the grid
-// barrier at the end of the layer is the only grid-wide synchronisation
-// (native-routing layers add one for the router logits).
+// a contiguous run of half-groups (shared-expert units with LoRA count
+// double).  Inside a team each CTA computes a slice of the SwiGLU activations
+// a = silu(G h) * (U h) for the team's rows and writes them into every team
+// member's shared memory (distributed shared memory); one cluster barrier
+// later every member holds the team's activations, quantises them, and
+// computes the partial down projection sum_k w_k D_k[:, team columns] a_k for
+// its share of the output rows.  The partial sums are added into the layer
+// output y with red.add; the grid barrier at the end of the layer is the only
+// grid-wide synchronisation (native-routing layers add one for the router
+// logits).
 //
 // Every CTA keeps the residual stream r in its own shared memory and
 // updates it from y at the start of the next layer, so the RMSNorm needs one
-// 8 KB read per CTA and no extra barrier.  The prerouter head runs on four
-// auxiliary warps per CTA alongside the expert warps: fc1 and the linear
-// residual of the owner layer l, fc2 of owner l-1 (its hidden vector is
-// complete once layer l starts), and the routing of owner l-2's logits.
-// Weights of layer l+1 are prefetched into L2 at the start of layer l; for
-// consumer layers the routed experts are known one token ahead (prediction
-// as routing), so their bytes are in flight long before they are used.
+// 8 KB read per CTA and no extra barrier.  The prerouter heads run on four
+// head warps per CTA alongside the eight expert warps (which join once their
+// down rows are done): fc2 of owner l-1 (its hidden vector is complete once
+// layer l starts), fc1 and the linear residual of owner l, and the routing
+// of owner l-2's logits.
+//
+// Each member's weight slices of a layer (gate/up row runs, down slices and
+// the LoRA operands) are copied into shared memory with bulk copies: for a
+// layer whose routing is a prediction made one token earlier, while the
+// previous layer still runs; for a native layer, right after its routing.
 // Included inside namespace e0 of e0_decode.cu (it uses StackHdr and the
 // phase helpers defined there).
 #pragma once
@@ -63,27 +67,6 @@ E0_DEV uint32_t cl_map(const void* local, uint32_t rank) {
 }
 E0_DEV void cl_st(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-E0_DEV void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// This CTA's 1/n share of a byte range, prefetched into L2.
-E0_DEV void prefetch_share(const void* base, size_t bytes, int b, int n) {
-    if (!base || bytes < 16) return;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(base) & ~(uintptr_t)15;
-    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base) + bytes + 15) & ~(uintptr_t)15;
-    const size_t total = a1 - a0;
-    size_t chunk = (total / n + 15) & ~(size_t)15;
-    if (chunk < 256) chunk = 256;
-    const size_t s0 = (size_t)b * chunk;
-    if (s0 >= total) return;
-    size_t len = total - s0 < chunk ? total - s0 : chunk;
-    for (size_t o = 0; o < len; o += 65536) {
-        const size_t piece = len - o < 65536 ? len - o : 65536;
-        prefetch_l2(reinterpret_cast<const void*>(a0 + s0 + o), (uint32_t)piece);
-    }
 }
 
 // ------------------------------------------------------------------ barrier
