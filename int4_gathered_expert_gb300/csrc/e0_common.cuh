@@ -103,10 +103,10 @@ E0_DEV float2 ld2_shared_or_l2(const float* p) {
 }
 E0_DEV int ldi_shared_or_l2(const int32_t* p) { return __isGlobal(p) ? __ldcg(p) : *p; }
 
-// One warp quantises group g of x (64 fp32 values) into planes + XGroup.
-// Plane word k of the group is stored at planes[k * pstride].
-E0_DEV void quantize_group_warp(const float* x, uint4* planes, XGroup* xg, int lane, uint32_t* st, int pstride = 1) {
-    const float2 v = ld2_shared_or_l2(x + 2 * lane);
+// One warp quantises one 64-value group (lane holds elements 2*lane and
+// 2*lane + 1) into planes + XGroup.  Plane word k of the group is stored at
+// planes[k * pstride].
+E0_DEV void quantize_group_v(const float2 v, uint4* planes, XGroup* xg, int lane, uint32_t* st, int pstride = 1) {
     float mx = warp_max(fmaxf(fabsf(v.x), fabsf(v.y)));
     if (!(mx < 3.0e38f)) {  // NaN or inf in the activations
         if (lane == 0) set_status(st, E0_ST_NONFINITE);
@@ -137,6 +137,11 @@ E0_DEV void quantize_group_warp(const float* x, uint4* planes, XGroup* xg, int l
         xg->c = mx / 32767.f;
         xg->sx = (float)s;
     }
+}
+
+// One warp quantises group g of x (64 fp32 values) into planes + XGroup.
+E0_DEV void quantize_group_warp(const float* x, uint4* planes, XGroup* xg, int lane, uint32_t* st, int pstride = 1) {
+    quantize_group_v(ld2_shared_or_l2(x + 2 * lane), planes, xg, lane, st, pstride);
 }
 
 // Partial dot product of one 64-element group of an int4 row (two uint4 code

@@ -539,7 +539,7 @@ __host__ __device__ inline void stage_need(int H, int I, int units, int rank, si
 // ------------------------------------------------------------------ shared memory layout
 
 struct T2Smem {
-    size_t hdr, lyr, r, h, hpl, hxg, ateam, apl, axg, zred, zg, zu, zd, inds, w, slots, scr, red, hnext, plan, bars, stage_gu,
+    size_t hdr, lyr, r, hpl, hxg, ateam, apl, axg, zred, zg, zu, zd, inds, w, slots, scr, red, hnext, plan, bars, stage_gu,
         stage_dn, dn_bytes, total;
     __host__ __device__ T2Smem(int H, int E, int L, int K, size_t gu_cap, size_t dn_cap) {
         const int GH = H / GROUP;
@@ -550,8 +550,6 @@ struct T2Smem {
         lyr = o;  // copy of the layer descriptors
         o += ((size_t)L * sizeof(LayerP) + 15) & ~(size_t)15;
         r = o;
-        o += (size_t)H * 4;
-        h = o;
         o += (size_t)H * 4;
         hpl = o;
         o += (size_t)GH * 8 * 16;
@@ -658,7 +656,6 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     const StackHdr& S = *reinterpret_cast<const StackHdr*>(smem + lay.hdr);
     const LayerP* lyr = reinterpret_cast<const LayerP*>(smem + lay.lyr);
     float* r = reinterpret_cast<float*>(smem + lay.r);
-    float* h = reinterpret_cast<float*>(smem + lay.h);
     uint4* hpl = reinterpret_cast<uint4*>(smem + lay.hpl);
     XGroup* hxg = reinterpret_cast<XGroup*>(smem + lay.hxg);
     float* ateam = reinterpret_cast<float*>(smem + lay.ateam);
@@ -779,47 +776,50 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         float* w_s = w_all + l * K;
         const uint8_t** slot_s = slot_all + l * (K + 1);
 
-        // ---- residual stream: r_l = x (l = 0) or r_{l-1} + y_{l-1}; h = RMSNorm(r)
+        // ---- residual stream r_l = x (l = 0) or r_{l-1} + y_{l-1}, and the planes
+        // of h = RMSNorm(r) = r / denom.  The int16 codes of a group do not
+        // change when the group is scaled, so each warp quantises its groups of
+        // r while it updates them, and every product with h is taken with r and
+        // scaled by inv_denom afterwards (planes, router, LoRA A, head rows):
+        // one pass and one block barrier.
+        float inv_denom;
         {
             const float* ysrc = l == 0 ? x : S.y_acc + (size_t)((l - 1) % 3) * H;
             float ss = 0.f;
-            for (int j = tid * 4; j < H; j += T2_THREADS * 4) {
-                const float4 y4 = __ldcg(reinterpret_cast<const float4*>(ysrc + j));
-                float4 v;
-                if (l == 0) {
-                    v = y4;
-                } else {
-                    const float4 r4 = *reinterpret_cast<const float4*>(r + j);
-                    v = make_float4(r4.x + y4.x, r4.y + y4.y, r4.z + y4.z, r4.w + y4.w);
+            for (int g = warp; g < GH; g += NW) {
+                const int j = GROUP * g + 2 * lane;
+                const float2 y2 = __ldcg(reinterpret_cast<const float2*>(ysrc + j));
+                float2 v = y2;
+                if (l > 0) {
+                    const float2 r2 = *reinterpret_cast<const float2*>(r + j);
+                    v = make_float2(r2.x + y2.x, r2.y + y2.y);
                 }
-                *reinterpret_cast<float4*>(r + j) = v;
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                ss = fmaf(v.z, v.z, ss);
-                ss = fmaf(v.w, v.w, ss);
+                *reinterpret_cast<float2*>(r + j) = v;
+                ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
+                // word k of group g sits at hpl[k * GH + g]: lanes that read
+                // consecutive groups touch consecutive 16-byte words
+                quantize_group_v(v, hpl + g, hxg + g, lane, nullptr, GH);
             }
             ss = warp_sum(ss);
             if (lane == 0) red[warp] = ss;
-            __syncthreads();
-            float tot = lane < NW ? red[lane] : 0.f;
-            tot = warp_sum(tot);
-            const float denom = sqrtf(tot / (float)H + 1e-6f);
-            for (int j = tid; j < H; j += T2_THREADS) h[j] = r[j] / denom;
-            if (b == 0 && tr.r)
-                for (int j = tid; j < H; j += T2_THREADS) tr.r[(size_t)l * H + j] = r[j];
             // this block's prerouter-head units of layer l start from the first
             if (tid == 0) *hnext = 0;
             // the output buffer of layer l+1 starts at zero
             if (b == nb - 1)
                 for (int j = tid; j < H; j += T2_THREADS) S.y_acc[(size_t)((l + 1) % 3) * H + j] = 0.f;
+            __syncthreads();
+            float tot = lane < NW ? red[lane] : 0.f;
+            tot = warp_sum(tot);
+            inv_denom = 1.f / sqrtf(tot / (float)H + 1e-6f);
+            if (b == 0 && tr.r)
+                for (int j = tid; j < H; j += T2_THREADS) tr.r[(size_t)l * H + j] = r[j];
         }
-        __syncthreads();
 
         // ---- routing of native layers: logits on every warp of the grid, one grid barrier
         if (native) {
             for (int e = b * NW + warp; e < E; e += nb * NW) {
-                const float acc = warp_sum(hrow_dot(L.W_r + (size_t)e * H, h, H, lane));
-                if (lane == 0) S.logits[e] = acc;
+                const float acc = warp_sum(hrow_dot(L.W_r + (size_t)e * H, r, H, lane));
+                if (lane == 0) S.logits[e] = acc * inv_denom;
             }
             grid_barrier2(Sp, bar0 + (unsigned long long)(++nbar) * nb, st);
             if (warp == 0) {
@@ -844,10 +844,6 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             if (tr.inds) tr.inds[(size_t)l * K + lane] = e;
             if (tr.w) tr.w[(size_t)l * K + lane] = w_s[lane];
         }
-        // planes of h: word k of group g sits at hpl[k * GH + g], so lanes that
-        // read consecutive groups touch consecutive 16-byte words
-        for (int g = warp; g < GH; g += NW) quantize_group_warp(h + GROUP * g, hpl + g, hxg + g, lane, nullptr, GH);
-        __syncthreads();
 
         const T2Split sp = split_of(l);
         const int p0 = (int)((long)crank * sp.rows / TEAM), p1 = (int)((long)(crank + 1) * sp.rows / TEAM);
@@ -867,7 +863,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                 float acc = 0.f;
                 // Am may point into a staging region: a generic load serves either space
                 for (int c = lane * 8; c < nc; c += 256)
-                    acc += h8_dot(*reinterpret_cast<const uint4*>(Am + c), h + c0 + c);
+                    acc += h8_dot(*reinterpret_cast<const uint4*>(Am + c), r + c0 + c);
                 acc = warp_sum(acc);
                 if (lane < TEAM) cl_st(cl_map(zred + crank * 2 * T2_MAX_RANK + rr, lane), acc);
             }
@@ -875,7 +871,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             for (int rr = tid; rr < 2 * rank; rr += T2_THREADS) {
                 float v = 0.f;
                 for (int m = 0; m < TEAM; ++m) v += zred[m * 2 * T2_MAX_RANK + rr];
-                (rr < rank ? zg : zu)[rr % rank] = v;
+                (rr < rank ? zg : zu)[rr % rank] = v * inv_denom;
             }
             __syncthreads();
         }
@@ -935,8 +931,8 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                         pg = q4_group_dot(c[v][0], c[v][1], hpl + rm.g, hxg[rm.g], sbv[v][0], GH);
                         pu = q4_group_dot(c[v][2], c[v][3], hpl + rm.g, hxg[rm.g], sbv[v][1], GH);
                     }
-                    pg = seg_sum(pg, rm.G, lane);
-                    pu = seg_sum(pu, rm.G, lane);
+                    pg = seg_sum(pg, rm.G, lane) * inv_denom;
+                    pu = seg_sum(pu, rm.G, lane) * inv_denom;
                     const int lead = lane - rm.g;
                     float a = 0.f;
                     if (lv[v] && rm.g == 0 && hv[v]) {
@@ -1068,7 +1064,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                     const int q = it - nA;
                     const __half* wr = q < n_fc1 ? L.fc1 + (size_t)q * ((size_t)H + 2 * E)
                                                  : L.lres + (size_t)(q - n_fc1) * ((size_t)H + 2 * E);
-                    float a0 = hrow_dot(wr, h, H, lane);
+                    float a0 = hrow_dot(wr, r, H, lane) * inv_denom;
                     // the one-hot columns: this layer's experts, then the previous token's
                     if (lane < 2 * K) {
                         const int e = lane < K ? inds_s[lane] : (prev ? __ldcg(prev + lane - K) : -1);
