@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--route-k", type=int, default=4, help="routed experts per token (the 35B tier uses 4)")
     p.add_argument("--no-prerouter", action="store_true",
                    help="every layer routes with its own router; no prerouter heads")
+    p.add_argument("--no-streaming", action="store_true", help="skip the host-tier staged-streaming measurement")
+    p.add_argument("--stream-split", type=int, default=22,
+                   help="first layer of the second launch of a token in the staged-streaming run")
     return p.parse_args()
 
 
@@ -112,6 +115,89 @@ def run_prefill_bench(dev, reps: int = 5, tier: str = "35b"):
                          "peak_source": "MEASURED_PEAKS.json bf16_tflops (measured, fp16 = bf16 rate)"
                          if pk else "fallback"},
             "l2": "flushed (256 MB write) before each timed call", "device_status": int(st.item())}
+
+
+# ---------------------------------------------------------------- host-tier staged streaming
+
+
+def run_streaming_bench(model, X, args, tps: int):
+    """Decode with the consumer layers' experts in pinned host memory and 2K
+    device slots per layer, filled with the prerouter's prediction one token
+    ahead (model.StreamedStack).  Reports tok/s with the copies overlapped on a
+    second stream, with the copies serialised on the compute stream, and with
+    the same two-launch token from the resident bank; plus the expert bytes
+    copied per token (measured from the slot pools' occupant tables)."""
+    import torch
+    from int4_gathered_expert_gb300.model import StackDev, StreamedStack
+    sd = StackDev(model, trace=False)
+    ss = StreamedStack(sd, split=args.stream_split)
+    n_tok = min(tps, X.shape[0] - 1)
+
+    def timed(fn, n):
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(ss.cs)
+        for i in range(n):
+            fn(i)
+        b.record(ss.cs)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3
+
+    ss.start(X[0])
+    # expert copies per token, from the occupant tables (untimed pass)
+    occ = {l: ss.pools[l].occupant.clone() for l in ss.staged}
+    n_count = min(16, n_tok)
+    copied = 0
+    for i in range(n_count):
+        ss.step(X[1 + i])
+        torch.cuda.synchronize()
+        for l in ss.staged:
+            now = ss.pools[l].occupant
+            copied += int((now != occ[l]).sum().item())
+            occ[l] = now.clone()
+    per_token_bytes = copied / n_count * ss.copy_bytes_per_expert()
+    base = 1 + n_count
+    n = max(1, min(n_tok, X.shape[0] - base) // 2)
+    t_overlap = timed(lambda i: ss.step(X[base + i], overlap=True), n)
+    t_serial = timed(lambda i: ss.step(X[base + n + i], overlap=False), n)
+    status = int(ss.status.item())
+    n_staged = len(ss.staged)
+    del ss, sd
+    torch.cuda.empty_cache()
+    # the same two launches per token from the resident bank
+    rd = StackDev(model, trace=False)
+    cs = torch.cuda.Stream()
+    L_ = rd.L
+    from int4_gathered_expert_gb300 import lib as L
+
+    def resident_token(i):
+        L.e0_stack_step_range(X[i], None, rd.ws, 0, args.stream_split, None, rd.status, stream=cs)
+        L.e0_stack_step_range(None, rd.r_out, rd.ws, args.stream_split, L_, None, rd.status, stream=cs)
+
+    for i in range(3):
+        resident_token(i)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(cs)
+    for i in range(n):
+        resident_token(3 + i)
+    b.record(cs)
+    torch.cuda.synchronize()
+    t_res = a.elapsed_time(b) / 1e3
+    del rd
+    torch.cuda.empty_cache()
+    exposed = max(0.0, t_serial - t_res)
+    return {"workload": "35B-tier stack decode with host-tier staged streaming: consumer layers hold 2K device "
+                        "slots filled from pinned host memory with the prediction one token ahead",
+            "tokens": n, "split": args.stream_split, "staged_layers": n_staged,
+            "tok_s_streamed_overlapped": n / t_overlap, "tok_s_streamed_serial": n / t_serial,
+            "tok_s_resident_two_launch": n / t_res,
+            "expert_bytes_copied_per_token": per_token_bytes,
+            "exposed_copy_us_per_token_serial": 1e6 * exposed / n,
+            "exposed_copy_us_per_token_overlapped": 1e6 * max(0.0, t_overlap - t_res) / n,
+            "device_status": status}
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -426,6 +512,16 @@ def run_gb300(args):
                "sample": f"first {n_cpu} tokens of the same stream (token 0 routes all 40 layers natively) "
                          "through the 40-layer stack, float64 numpy oracle"}
 
+    streaming = None
+    if rank == 0 and not args.no_streaming and args.kernel_impl == 2:
+        del sd
+        torch.cuda.empty_cache()
+        try:
+            streaming = run_streaming_bench(model, X, args, tps)
+        except Exception as ex:  # a measurement that cannot run here is reported, not fatal
+            streaming = {"error": repr(ex)[:300]}
+        sd = None
+
     prefill = prefill8 = None
     if rank == 0 and not args.no_prefill:
         del sd
@@ -455,7 +551,7 @@ def run_gb300(args):
                              "frac": achieved / peak, "traffic": traffic,
                              "kernel": kname, "launch_us": mean_launch_s * 1e6,
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback"},
-                "cpu_baseline": cpu, "e2e": e2e, "prefill": prefill, "prefill_8b": prefill8, "gpu_launches": n_timed * LAUNCHES_PER_TOKEN.get(args.kernel_impl, 6 * shape.n_layers + 1),
+                "cpu_baseline": cpu, "e2e": e2e, "prefill": prefill, "prefill_8b": prefill8, "streaming": streaming, "gpu_launches": n_timed * LAUNCHES_PER_TOKEN.get(args.kernel_impl, 6 * shape.n_layers + 1),
                 "clocks": clocks, "device_status": st}
         print(json.dumps(line), flush=True)
     if ws > 1:

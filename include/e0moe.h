@@ -319,6 +319,37 @@ int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
 int e0_stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* trace,
                   int impl, uint32_t* d_status, e0_stream_t stream);
 
+/* ---- staged streaming of predicted experts ------------------------------ */
+
+/* Layers [layer_begin, layer_end) of the current token with the cluster
+ * kernel (impl 2).  A token is the launches whose ranges cover 0..L in order
+ * on one stream; x is read by the range that starts at 0, r_out written by
+ * the range that ends at L (the token counter advances there).  Between the
+ * launches of a token the caller may run other work on other streams, e.g.
+ * e0_stack_prefetch_experts for layers whose prediction for the next token
+ * is already final.  ([KOALA] §1-§2, [JAEHUN] §3.1: the prediction made one
+ * token ahead is what lets the load of the next token's experts overlap the
+ * current token.)  Errors: unknown workspace or empty / out-of-range layer
+ * range -> E0_ERR_ARG; no cluster geometry -> E0_ERR_UNSUPPORTED. */
+int e0_stack_step_range(const float* x, float* r_out, void* ws, int layer_begin, int layer_end,
+                        const e0_stack_trace* trace, uint32_t* d_status, e0_stream_t stream);
+
+/* Replace the layer descriptors of a prepared stack (e.g. move a layer from
+ * the resident bank to a staged slot pool) keeping its routing history,
+ * predictions and token counter.  Each layer must keep its configuration
+ * (shared expert, LoRA rank, head, consumer flag) -> else E0_ERR_ARG.
+ * Synchronises the stream. */
+int e0_stack_update_layers(void* ws, const e0_stack_layer* layers, int L, e0_stream_t stream);
+
+/* Bring the K experts the prerouter predicted for token t_next (>= 1) of
+ * `layer` into `pool` (a staged slot pool whose table the layer's descriptor
+ * uses): e0_slot_update from `bank` (the layer's experts in kernel layout,
+ * device or host memory the GPU can read, slot i = expert i) with the
+ * prediction as the next set.  Valid once the prediction is final: after the
+ * launch that ran layer + 1 of token t_next - 1 (or that token's last layer). */
+int e0_stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank,
+                              uint32_t* d_status, e0_stream_t stream);
+
 /* ---- whole-layer prefill (sorted gather + tcgen05 grouped GEMM) ------- */
 
 /* Group the T*K assignments (t, k) by expert ([PTKR] "SSD 전문가 스트리밍":

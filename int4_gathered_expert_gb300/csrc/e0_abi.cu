@@ -233,6 +233,33 @@ int e0_moe_prefill_forward(const uint16_t* X, int T, const e0_slot_pool* bank, c
     return e0::moe_prefill_forward(X, T, bank, W_router, rp, Y, inds_out, w_out, ws, d_status, cs(stream));
 }
 
+int e0_stack_step_range(const float* x, float* r_out, void* ws, int layer_begin, int layer_end,
+                        const e0_stack_trace* trace, uint32_t* d_status, e0_stream_t stream) {
+    if (!ws) return E0_ERR_NULL;
+    if (!e0::stack_known(ws)) return E0_ERR_ARG;
+    if (layer_begin == 0 && !x) return E0_ERR_NULL;
+    return e0::stack_step_range(x, r_out, ws, layer_begin, layer_end, trace, d_status, cs(stream));
+}
+
+int e0_stack_update_layers(void* ws, const e0_stack_layer* layers, int L, e0_stream_t stream) {
+    if (!ws || !layers) return E0_ERR_NULL;
+    if (!e0::stack_known(ws)) return E0_ERR_ARG;
+    for (int l = 0; l < L; ++l) {
+        const int rc = check_pool(&layers[l].pool);
+        if (rc != E0_OK) return rc;
+    }
+    return e0::stack_update_layers(ws, layers, L, cs(stream));
+}
+
+int e0_stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank,
+                              uint32_t* d_status, e0_stream_t stream) {
+    if (!ws || !pool || !bank) return E0_ERR_NULL;
+    if (!e0::stack_known(ws)) return E0_ERR_ARG;
+    const int rc = check_pool(pool);
+    if (rc != E0_OK) return rc;
+    return e0::stack_prefetch_experts(ws, layer, t_next, pool, bank, d_status, cs(stream));
+}
+
 int e0_selftest_bounded_wait(const uint32_t* flag, uint32_t limit_us, uint32_t* d_status, e0_stream_t stream) {
     if (!flag || !d_status) return E0_ERR_NULL;
     if (limit_us == 0 || limit_us > E0_SELFTEST_MAX_WAIT_US) return E0_ERR_ARG;

@@ -971,6 +971,100 @@ bool stack_known(const void* ws) {
     return g_stacks.count(ws) != 0;
 }
 
+static TraceP trace_of(const e0_stack_trace* trace) {
+    TraceP tr;
+    memset(&tr, 0, sizeof(tr));
+    if (trace) {
+        tr.r = trace->r;
+        tr.inds = trace->inds;
+        tr.w = trace->w;
+        tr.head_logits = trace->head_logits;
+        tr.pred_inds = trace->pred_inds;
+    }
+    return tr;
+}
+
+static bool stack_hdr(const void* ws, StackHdr* out) {
+    std::lock_guard<std::mutex> g(g_stack_mu);
+    auto it = g_stacks.find(ws);
+    if (it == g_stacks.end()) return false;
+    *out = it->second;
+    return true;
+}
+
+// Layers [lb, le) of the current token with the cluster kernel.
+int stack_step_range(const float* x, float* r_out, void* ws, int lb, int le, const e0_stack_trace* trace, uint32_t* st,
+                     cudaStream_t s) {
+    num_sms();
+    StackHdr* Sp = reinterpret_cast<StackHdr*>(ws);
+    StackHdr hdr;
+    if (!stack_hdr(ws, &hdr)) return E0_ERR_ARG;
+    if (lb < 0 || le > hdr.L || lb >= le) return E0_ERR_ARG;
+    if (le == hdr.L && !r_out) return E0_ERR_NULL;
+    if (hdr.teams < 1) return E0_ERR_UNSUPPORTED;
+    const TraceP tr = trace_of(trace);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(hdr.grid2);
+    cfg.blockDim = dim3(T2_THREADS);
+    cfg.dynamicSmemBytes = (size_t)hdr.smem2;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = TEAM;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeCooperative;
+    at[1].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_stack_token2, Sp, x, r_out, tr, st, lb, le);
+    if (e != cudaSuccess) {
+        // co-residency of a grid that fits on the device at once without the cooperative attribute
+        cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, k_stack_token2, Sp, x, r_out, tr, st, lb, le);
+    }
+    return cuda_ok(e);
+}
+
+// New layer descriptors for a prepared stack, keeping its routing history,
+// predictions and token counter; the layers' configuration must not change.
+int stack_update_layers(void* ws, const e0_stack_layer* layers, int L, cudaStream_t s) {
+    StackHdr hdr;
+    if (!stack_hdr(ws, &hdr)) return E0_ERR_ARG;
+    if (L != hdr.L) return E0_ERR_ARG;
+    LayerP* hl = new LayerP[L];
+    LayerP* cur = new LayerP[L];
+    int rc = E0_OK;
+    if (cudaMemcpyAsync(cur, hdr.layers, sizeof(LayerP) * L, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        rc = E0_ERR_CUDA;
+    for (int l = 0; l < L && rc == E0_OK; ++l) {
+        hl[l] = to_layer(&layers[l].pool, layers[l].W_router, layers[l].shared, layers[l].head, layers[l].consumer);
+        const bool same = (hl[l].sh != nullptr) == (cur[l].sh != nullptr) && (hl[l].Ag != nullptr) == (cur[l].Ag != nullptr) &&
+                          hl[l].rank == cur[l].rank && (hl[l].fc1 != nullptr) == (cur[l].fc1 != nullptr) &&
+                          hl[l].hidden == cur[l].hidden && hl[l].consumer == cur[l].consumer;
+        if (!same) rc = E0_ERR_ARG;
+    }
+    if (rc == E0_OK && (cudaMemcpyAsync(hdr.layers, hl, sizeof(LayerP) * L, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+                        cudaStreamSynchronize(s) != cudaSuccess))
+        rc = E0_ERR_CUDA;
+    delete[] hl;
+    delete[] cur;
+    return rc;
+}
+
+// Bring the experts predicted for token t_next of `layer` into `pool`.
+int stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank, uint32_t* st,
+                           cudaStream_t s) {
+    StackHdr hdr;
+    if (!stack_hdr(ws, &hdr)) return E0_ERR_ARG;
+    if (layer < 0 || layer >= hdr.L || t_next < 1) return E0_ERR_ARG;
+    const int32_t* next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
+    return slot_update(pool, next, hdr.K, nullptr, 0, bank, st, s);
+}
+
 int stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* trace, int impl, uint32_t* st,
                cudaStream_t s) {
     num_sms();
@@ -991,32 +1085,7 @@ int stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* tra
         tr.head_logits = trace->head_logits;
         tr.pred_inds = trace->pred_inds;
     }
-    if (impl == 2) {
-        if (hdr.teams < 1) return E0_ERR_UNSUPPORTED;
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof(cfg));
-        cfg.gridDim = dim3(hdr.grid2);
-        cfg.blockDim = dim3(T2_THREADS);
-        cfg.dynamicSmemBytes = (size_t)hdr.smem2;
-        cfg.stream = s;
-        cudaLaunchAttribute at[2];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = TEAM;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        at[1].id = cudaLaunchAttributeCooperative;
-        at[1].val.cooperative = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 2;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, k_stack_token2, Sp, x, r_out, tr, st);
-        if (e != cudaSuccess) {
-            // co-residency of a grid that fits on the device at once without the cooperative attribute
-            cudaGetLastError();
-            cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, k_stack_token2, Sp, x, r_out, tr, st);
-        }
-        return cuda_ok(e);
-    }
+    if (impl == 2) return stack_step_range(x, r_out, ws, 0, hdr.L, trace, st, s);
     if (impl == 0) {
         const PersistSmem lay(hdr.H, hdr.E, hdr.K, (size_t)hdr.smem);
         void* args[] = {&Sp, (void*)&x, &r_out, &tr, &st};

@@ -16,6 +16,16 @@ int pack_experts(const e0_expert_q* src, int n, const e0_slot_pool* dst, const i
                  const int32_t* expert_ids, cudaStream_t s);
 int slot_update(const e0_slot_pool* p, const int32_t* next, int n_next, const int32_t* cur, int n_cur,
                 const uint8_t* bank, uint32_t* st, cudaStream_t s);
+int stack_step_range(const float* x, float* r_out, void* ws, int lb, int le, const e0_stack_trace* trace, uint32_t* st,
+                     cudaStream_t s);
+int stack_update_layers(void* ws, const e0_stack_layer* layers, int L, cudaStream_t s);
+int stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank, uint32_t* st,
+                           cudaStream_t s);
+int stack_step_range(const float* x, float* r_out, void* ws, int lb, int le, const e0_stack_trace* trace, uint32_t* st,
+                     cudaStream_t s);
+int stack_update_layers(void* ws, const e0_stack_layer* layers, int L, cudaStream_t s);
+int stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank, uint32_t* st,
+                           cudaStream_t s);
 int route(const float* logits, int T, int E, const e0_route_params* rp, int32_t* inds, float* w, uint32_t* st,
           cudaStream_t s);
 int rmsnorm(const float* r, int T, int H, float eps, float* h, cudaStream_t s);

@@ -334,10 +334,18 @@ E0_DEV void mbar_expect2(uint64_t* bar, uint32_t bytes) {
                  "r"(bytes)
                  : "memory");
 }
-// Bounded wait for a staging barrier's phase; false when it gave up.
+// Bounded wait for a staging barrier's phase: gives up (false) after 50 ms of
+// device time; a copy of a few hundred KB lands in microseconds.
 E0_DEV bool mbar_wait2(uint64_t* bar, uint32_t parity) {
     const uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
-    for (uint32_t it = 0; it < (1u << 22); ++it) {
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (uint32_t it = 0;; ++it) {
+        if ((it & 63) == 63) {
+            uint64_t t1;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+            if (t1 - t0 > 50000000ull) return false;
+        }
         uint32_t ok;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
@@ -628,7 +636,7 @@ struct T2Split {
 // ------------------------------------------------------------------ the kernel
 
 __global__ void __launch_bounds__(T2_THREADS, 1)
-    k_stack_token2(StackHdr* Sp, const float* x, float* r_out, TraceP tr, uint32_t* st) {
+    k_stack_token2(StackHdr* Sp, const float* x, float* r_out, TraceP tr, uint32_t* st, int lb, int le) {
     extern __shared__ __align__(16) char smem[];
     const int H = Sp->H, I = Sp->I, E = Sp->E, K = Sp->K, Lz = Sp->L;
     const int GH = H / GROUP;
@@ -712,8 +720,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         return T2Split(I, K, Lq.sh != nullptr, Lq.sh != nullptr && Lq.Ag != nullptr, team, NT);
     };
     // Staging.  The gate/up region holds one layer at a time and completes once
-    // per layer (layer l waits on parity l & 1); the down regions alternate by
-    // layer parity (layer l waits on region l & 1, parity (l >> 1) & 1).  A
+    // per layer (layer l waits on parity (l - lb) & 1, counting from the first
+    // layer of this launch); the down regions alternate by layer parity (layer
+    // l waits on region l & 1, parity ((l - lb) >> 1) & 1).  A
     // layer whose routing is known when the token starts is copied while the
     // layer before it runs: its down side when that layer starts, its gate/up
     // side once that layer's gate/up rows have been read.  A native layer is
@@ -761,12 +770,18 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         stage_issue(&plan.dnt, slot_all + l * (K + 1), K, lora_ptrs(l), stage_dn_buf + (size_t)b * lay.dn_bytes,
                     plan.dn[b], &sbar[1 + b], lane);
     };
-    if (warp == HW && !layer_native(S, lyr[0], t)) {
-        stage_gu_for(0);
-        stage_dn_for(0);
+    if (warp == HW && !layer_native(S, lyr[lb], t)) {
+        stage_gu_for(lb);
+        stage_dn_for(lb);
+    }
+    // a launch that starts inside the token picks up the residual stream the
+    // previous launch of this token left in the header
+    if (lb > 0) {
+        for (int j = tid; j < H; j += T2_THREADS) r[j] = __ldcg(S.r + j);
+        __syncthreads();
     }
 
-    for (int l = 0; l < Lz; ++l) {
+    for (int l = lb; l < le; ++l) {
         const LayerP& L = lyr[l];
         const bool native = layer_native(S, L, t);
         const bool sh = L.sh != nullptr;
@@ -848,7 +863,9 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         const T2Split sp = split_of(l);
         const int p0 = (int)((long)crank * sp.rows / TEAM), p1 = (int)((long)(crank + 1) * sp.rows / TEAM);
         const bool team_lora = lora && sp.u1 > K * sp.HG;
-        const bool next_known = l + 1 < Lz && !layer_native(S, lyr[l + 1], t);
+        // the next layer's slices are copied ahead only when it runs in this
+        // launch: every bulk copy is waited for before the CTA exits
+        const bool next_known = l + 1 < le && !layer_native(S, lyr[l + 1], t);
         const int ps_m = max(p0, (K * sp.HG - sp.u0) * 32);  // this member's first shared-expert position
         const int db = l & 1;  // down region of this layer
 
@@ -856,7 +873,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         // member reduces 1/TEAM of the inputs, partial sums exchanged
         if (team_lora) {
             const int c0 = crank * (H / TEAM), nc = H / TEAM;
-            if (!mbar_wait2(&sbar[0], l & 1)) set_status(st, E0_ST_TIMEOUT);
+            if (!mbar_wait2(&sbar[0], (l - lb) & 1)) set_status(st, E0_ST_TIMEOUT);
             for (int rr = warp; rr < 2 * rank; rr += NW) {
                 const __half* Am =
                     plan.ag(0) ? plan.ag(rr) : (rr < rank ? L.Ag : L.Au) + (size_t)(rr % rank) * H + c0;
@@ -877,7 +894,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         }
 
         if (warp < T2_EXPERT_W) {
-            if (!mbar_wait2(&sbar[0], l & 1)) set_status(st, E0_ST_TIMEOUT);
+            if (!mbar_wait2(&sbar[0], (l - lb) & 1)) set_status(st, E0_ST_TIMEOUT);
             // ---- gate/up rows of this member, a = silu(G h) * (U h), stored into every member
             const RowMap rm(H, lane);
             const int step = T2_EXPERT_W * rm.R;
@@ -961,7 +978,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             asm volatile("bar.arrive 2, %0;" ::"r"(T2_EXPERT_W * 32 + 32));
             // ---- team exchange of the activations
             cl_sync();
-            if (!mbar_wait2(&sbar[1 + (l & 1)], (l >> 1) & 1)) set_status(st, E0_ST_TIMEOUT);
+            if (!mbar_wait2(&sbar[1 + (l & 1)], ((l - lb) >> 1) & 1)) set_status(st, E0_ST_TIMEOUT);
             // quantise the team's activations (one half-group per warp) and the
             // LoRA B input zd = A_down[:, team cols] . a_s of the shared rows
             const int nu = sp.u1 - sp.u0;
@@ -1091,6 +1108,14 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         grid_barrier2(Sp, bar0 + (unsigned long long)(++nbar) * nb, st);
     }
 
+    if (le < Lz) {
+        // ---- the token continues in another launch: hand over r_{le-1}
+        if (b == 0) {
+            for (int j = tid; j < H; j += T2_THREADS) S.r[j] = r[j];
+            if (tid == 0) Sp->bar_base = bar0 + (unsigned long long)nbar * nb;
+        }
+        return;
+    }
     // ---- token output, the last pending prediction, bookkeeping
     if (b == 0) {
         const float* ysrc = S.y_acc + (size_t)((Lz - 1) % 3) * H;

@@ -93,6 +93,9 @@ def load() -> C.CDLL:
         "e0_stack_prepare": (C.c_int, [P(StackLayer), C.c_int, C.c_int, C.c_int, C.c_int, P(RouteParams),
                                        vp, sz, vp]),
         "e0_stack_step": (C.c_int, [vp, vp, vp, P(StackTrace), C.c_int, vp, vp]),
+        "e0_stack_step_range": (C.c_int, [vp, vp, vp, C.c_int, C.c_int, P(StackTrace), vp, vp]),
+        "e0_stack_update_layers": (C.c_int, [vp, P(StackLayer), C.c_int, vp]),
+        "e0_stack_prefetch_experts": (C.c_int, [vp, C.c_int, C.c_int, P(SlotPool), vp, vp, vp]),
         "e0_prefill_sort": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, vp, vp, vp, vp, sz, vp]),
         "e0_moe_prefill_forward": (C.c_int, [vp, C.c_int, P(SlotPool), vp, P(RouteParams), vp, vp, vp,
                                              vp, sz, vp, vp]),
@@ -113,7 +116,8 @@ def exported_symbols():
     return ["e0_slot_bytes", "e0_workspace_size", "e0_pack_experts", "e0_slot_update", "e0_route_softmax_topk",
             "e0_route_sigmoid_group", "e0_rmsnorm", "e0_moe_block_forward", "e0_moe_block_forward_noalloc",
             "e0_prerouter_forward",
-            "e0_stack_workspace_size", "e0_stack_prepare", "e0_stack_step", "e0_prefill_sort",
+            "e0_stack_workspace_size", "e0_stack_prepare", "e0_stack_step", "e0_stack_step_range",
+            "e0_stack_update_layers", "e0_stack_prefetch_experts", "e0_prefill_sort",
             "e0_moe_prefill_forward", "e0_selftest_bounded_wait", "e0_read_status", "e0_status_string"]
 
 
@@ -241,6 +245,26 @@ def e0_stack_step(x, r_out, ws, trace: Optional[StackTrace] = None, impl=0, stat
     tr = C.byref(trace) if trace is not None else None
     rc = load().e0_stack_step(ptr(x), ptr(r_out), ptr(ws), tr, impl, ptr(status), stream_handle(stream))
     return _check("e0_stack_step", rc, raise_on_error)
+
+
+def e0_stack_step_range(x, r_out, ws, layer_begin, layer_end, trace: Optional[StackTrace] = None, status=None,
+                        stream=None, raise_on_error=True):
+    tr = C.byref(trace) if trace is not None else None
+    rc = load().e0_stack_step_range(ptr(x), ptr(r_out), ptr(ws), int(layer_begin), int(layer_end), tr, ptr(status),
+                                    stream_handle(stream))
+    return _check("e0_stack_step_range", rc, raise_on_error)
+
+
+def e0_stack_update_layers(ws, layers, stream=None, raise_on_error=True):
+    arr = (StackLayer * len(layers))(*layers)
+    rc = load().e0_stack_update_layers(ptr(ws), arr, len(layers), stream_handle(stream))
+    return _check("e0_stack_update_layers", rc, raise_on_error)
+
+
+def e0_stack_prefetch_experts(ws, layer, t_next, pool: SlotPool, bank, status=None, stream=None, raise_on_error=True):
+    rc = load().e0_stack_prefetch_experts(ptr(ws), int(layer), int(t_next), C.byref(pool), ptr(bank), ptr(status),
+                                          stream_handle(stream))
+    return _check("e0_stack_prefetch_experts", rc, raise_on_error)
 
 
 def e0_prefill_sort(inds, T, K, E, counts, offsets, perm, ws, ws_bytes, stream=None, raise_on_error=True):

@@ -139,3 +139,93 @@ class StackDev:
         out = self.r_out if out is None else out
         L.e0_stack_step(x, out, self.ws, self.trace, impl, self.status, stream=stream)
         return out
+
+
+class StreamedStack:
+    """Host-tier staged streaming on top of a StackDev (cluster kernel).
+
+    Each staged layer keeps its experts (kernel layout) in pinned host memory
+    and only 2K slots in device memory.  A token runs as two launches, layers
+    [0, split) and [split, L); the experts the prerouter predicted for the next
+    token are copied host -> device by e0_stack_prefetch_experts on a second
+    stream: layers below split - 1 while the second half of the token runs,
+    layers from split on while the first half of the next token runs.  Layer
+    split - 1, whose prediction is final only once the token has ended but
+    which the next token's first half uses, stays in the resident bank, as do
+    the layers that route natively."""
+
+    def __init__(self, sd: "StackDev", split: int, device="cuda"):
+        self.sd = sd
+        self.split = split
+        consumers = [l for l in range(sd.L) if sd.layers[l].consumer]
+        self.batch1 = [l for l in consumers if l <= split - 2]
+        self.batch2 = [l for l in consumers if l >= split]
+        self.staged = self.batch1 + self.batch2
+        self.host = {}
+        self.pools = {}
+        n_slots = 2 * sd.K
+        for l in self.staged:
+            src = sd.pools[l].data
+            h = torch.empty(src.shape, dtype=torch.uint8, pin_memory=True)
+            h.copy_(src)
+            self.host[l] = h
+            self.pools[l] = SlotPoolDev(sd.H, sd.I, sd.E, n_slots, device)
+        torch.cuda.synchronize()
+        self.cs = torch.cuda.Stream()
+        self.ps = torch.cuda.Stream()
+        self.ev1 = torch.cuda.Event()
+        self.ev2 = torch.cuda.Event()
+        self.status = sd.status
+        self.t = 0
+
+    def copy_bytes_per_expert(self) -> int:
+        return L.e0_slot_bytes(self.sd.H, self.sd.I)
+
+    def _prefetch(self, layers, t_next, stream):
+        for l in layers:
+            L.e0_stack_prefetch_experts(self.sd.ws, l, t_next, self.pools[l].desc, self.host[l], self.status,
+                                        stream=stream)
+
+    def start(self, x0: torch.Tensor, out: Optional[torch.Tensor] = None):
+        """Token 0 (every layer routes natively) from the resident bank, then the
+        staged layers switch to their slot pools holding the predicted experts
+        of token 1."""
+        sd = self.sd
+        out = sd.r_out if out is None else out
+        with torch.cuda.stream(self.cs):
+            L.e0_stack_step_range(x0, out, sd.ws, 0, sd.L, sd.trace, self.status, stream=self.cs)
+            self._prefetch(self.staged, 1, self.cs)
+        self.cs.synchronize()
+        layers = list(sd.layers)
+        for l in self.staged:
+            layers[l] = L.StackLayer(self.pools[l].desc, layers[l].W_router, layers[l].shared, layers[l].head,
+                                     layers[l].consumer)
+        L.e0_stack_update_layers(sd.ws, layers, stream=self.cs)
+        self.layers = layers
+        self.ev1.record(self.cs)
+        self.ev2.record(self.cs)
+        self.t = 1
+        return out
+
+    def step(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, overlap: bool = True):
+        """Token self.t; the copies for token self.t + 1 are issued behind it."""
+        sd = self.sd
+        out = sd.r_out if out is None else out
+        t = self.t
+        cs, ps = self.cs, (self.ps if overlap else self.cs)
+        cs.wait_event(self.ev1)
+        L.e0_stack_step_range(x, None, sd.ws, 0, self.split, sd.trace, self.status, stream=cs)
+        ev_a = torch.cuda.Event()
+        ev_a.record(cs)
+        ps.wait_event(ev_a)
+        self._prefetch(self.batch1, t + 1, ps)
+        self.ev1.record(ps)
+        cs.wait_event(self.ev2)
+        L.e0_stack_step_range(None, out, sd.ws, self.split, sd.L, sd.trace, self.status, stream=cs)
+        ev_b = torch.cuda.Event()
+        ev_b.record(cs)
+        ps.wait_event(ev_b)
+        self._prefetch(self.batch2, t + 1, ps)
+        self.ev2.record(ps)
+        self.t = t + 1
+        return out
