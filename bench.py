@@ -5,9 +5,17 @@ One step = 256 consecutive decode tokens of an AR(1) token stream through the
 40 layers (H=2048, I=512, E=256, softmax-top-4, shared expert with an
 unmerged rank-16 LoRA, 33 prerouter heads owned by layers 6..38 whose
 predictions route layers 7..39 one token later).  Each token is one launch of
-the persistent whole-token kernel.  Weights are synthetic (seeded), resident in
-HBM (18.1 GB expert bank); every token streams ~484 MB of weights, far more
-than the 129 MB L2, so no flush is needed between iterations.
+the cluster whole-token kernel (--kernel-impl 2; 0 = persistent cooperative
+kernel, 1 = per-phase chain).  Weights are synthetic (seeded), resident in HBM
+(18.1 GB expert bank); every token streams ~484 MB of weights, far more than
+the 129 MB L2, so no flush is needed between iterations.
+
+The same JSON line also carries: the end-to-end rate through the C ABI with
+host buffers (e2e), the CPU oracle (cpu_baseline), the host-tier staged
+streaming run (streaming: consumer layers' experts in pinned host memory,
+copied one token ahead of use), and the T=4096 whole-layer prefill of the
+35B and the 8B tier (prefill, prefill_8b).  --route-k and --no-prerouter give
+the K / prerouter variants.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
