@@ -171,10 +171,12 @@ def run_streaming_bench(model, X, args, tps: int):
     t_serial = timed(lambda i: ss.step(X[base + n + i], overlap=False), n)
     status = int(ss.status.item())
     n_staged = len(ss.staged)
-    del ss, sd
+    host = ss.host
+    del ss
     torch.cuda.empty_cache()
     # the same two launches per token from the resident bank
-    rd = StackDev(model, trace=False)
+    rd = sd
+    rd.prepare()
     cs = torch.cuda.Stream()
     L_ = rd.L
     from int4_gathered_expert_gb300 import lib as L
@@ -194,11 +196,40 @@ def run_streaming_bench(model, X, args, tps: int):
     b.record(cs)
     torch.cuda.synchronize()
     t_res = a.elapsed_time(b) / 1e3
-    del rd
-    torch.cuda.empty_cache()
     exposed = max(0.0, t_serial - t_res)
+    # the same streaming with a cross-layer LRU cache of bundles in device memory in front of the host bank
+    caches = {}
+    for cap in (64, 1024):
+        from int4_gathered_expert_gb300.model import ExpertCacheDev
+        sd.prepare()
+        cache = ExpertCacheDev(cap, sd.L, sd.H, sd.I, sd.E)
+        ssc = StreamedStack(sd, split=args.stream_split, cache=cache, host=host)
+        ssc.start(X[0])
+        for i in range(8):  # warm the cache
+            ssc.step(X[1 + i])
+        torch.cuda.synchronize()
+        c0 = cache.stats()
+        torch.cuda.synchronize()
+        a2 = torch.cuda.Event(enable_timing=True)
+        b2 = torch.cuda.Event(enable_timing=True)
+        a2.record(ssc.cs)
+        for i in range(n):
+            ssc.step(X[9 + i], overlap=True)
+        b2.record(ssc.cs)
+        torch.cuda.synchronize()
+        tc = a2.elapsed_time(b2) / 1e3
+        c1 = cache.stats()
+        hits, misses = c1["hits"] - c0["hits"], c1["misses"] - c0["misses"]
+        caches[str(cap)] = {"tok_s_streamed_overlapped": n / tc, "hit_rate": hits / max(1, hits + misses),
+                            "host_bytes_per_token": misses / n * ssc.copy_bytes_per_expert(),
+                            "device_status": int(ssc.status.item())}
+        del ssc, cache
+        torch.cuda.empty_cache()
+    del sd, host
+    torch.cuda.empty_cache()
     return {"workload": "35B-tier stack decode with host-tier staged streaming: consumer layers hold 2K device "
                         "slots filled from pinned host memory with the prediction one token ahead",
+            "expert_cache": caches,
             "tokens": n, "split": args.stream_split, "staged_layers": n_staged,
             "tok_s_streamed_overlapped": n / t_overlap, "tok_s_streamed_serial": n / t_serial,
             "tok_s_resident_two_launch": n / t_res,

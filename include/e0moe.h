@@ -350,6 +350,31 @@ int e0_stack_update_layers(void* ws, const e0_stack_layer* layers, int L, e0_str
 int e0_stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank,
                               uint32_t* d_status, e0_stream_t stream);
 
+/* A cross-layer cache of expert bundles in device memory, least recently used
+ * first out ([PTKR] "SSD 전문가 스트리밍" / P2 `SharedExpertCache`: a hot set
+ * shared by all layers; misses go to the exact path, here the host bank).
+ * Keys are layer * E + expert.  All arrays are device memory owned by the
+ * caller and start as: key = -1, stamp = 0, map = -1, counters = 0. */
+typedef struct e0_expert_cache {
+    uint8_t* data;        /* capacity * e0_slot_bytes(H, I) bytes              */
+    int32_t* key;         /* [capacity] key held by each entry, -1 = empty      */
+    uint32_t* stamp;      /* [capacity] last use (a counter), 0 = never         */
+    int32_t* map;         /* [n_keys] key -> entry, -1 = not cached             */
+    uint32_t* counters;   /* [4]: clock, hits, misses, evictions                */
+    int32_t* scratch;     /* [4 + 4 * E0_MAX_K] plan of one prefetch           */
+    int32_t capacity, n_keys;
+} e0_expert_cache;
+
+/* e0_stack_prefetch_experts with a cross-layer cache in front of `bank`: a
+ * predicted expert missing from the layer's pool is copied from its cache
+ * entry when it has one (device to device), else from `bank` — and then also
+ * into the least recently used cache entry.  Hits, misses and evictions are
+ * counted in cache->counters.  Errors as e0_stack_prefetch_experts; a layer
+ * * E key beyond n_keys -> E0_ERR_ARG. */
+int e0_stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot_pool* pool,
+                                     const uint8_t* bank, const e0_expert_cache* cache,
+                                     uint32_t* d_status, e0_stream_t stream);
+
 /* ---- whole-layer prefill (sorted gather + tcgen05 grouped GEMM) ------- */
 
 /* Group the T*K assignments (t, k) by expert ([PTKR] "SSD 전문가 스트리밍":

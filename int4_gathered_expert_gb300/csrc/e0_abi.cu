@@ -260,6 +260,19 @@ int e0_stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_poo
     return e0::stack_prefetch_experts(ws, layer, t_next, pool, bank, d_status, cs(stream));
 }
 
+int e0_stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank,
+                                     const e0_expert_cache* cache, uint32_t* d_status, e0_stream_t stream) {
+    if (!ws || !pool || !bank || !cache) return E0_ERR_NULL;
+    if (!e0::stack_known(ws)) return E0_ERR_ARG;
+    const int rc = check_pool(pool);
+    if (rc != E0_OK) return rc;
+    if (cache->capacity < 0 || cache->n_keys < 1) return E0_ERR_ARG;
+    if (!cache->key || !cache->stamp || !cache->map || !cache->counters || !cache->scratch ||
+        (cache->capacity > 0 && !cache->data))
+        return E0_ERR_NULL;
+    return e0::stack_prefetch_experts_cached(ws, layer, t_next, pool, bank, cache, d_status, cs(stream));
+}
+
 int e0_selftest_bounded_wait(const uint32_t* flag, uint32_t limit_us, uint32_t* d_status, e0_stream_t stream) {
     if (!flag || !d_status) return E0_ERR_NULL;
     if (limit_us == 0 || limit_us > E0_SELFTEST_MAX_WAIT_US) return E0_ERR_ARG;

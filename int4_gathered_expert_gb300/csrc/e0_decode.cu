@@ -140,6 +140,99 @@ __global__ void k_slot_commit(int32_t* table, int32_t* occupant, int n_slots, in
     if (P.status) set_status(st, P.status);
 }
 
+// ================================================================== cross-layer expert cache
+
+// Plan layout in cache->scratch: [0] n copies, then per copy i (4 ints at
+// 4 + 4 i): expert, slot, source entry (-1: the bank), cache entry to fill
+// (-1: none).  One thread plans and updates the cache bookkeeping; the copy
+// kernel and the commit follow in stream order.
+__global__ void k_cache_plan(const int32_t* table, const int32_t* occupant, int n_slots, int E, const int32_t* next,
+                             int n_next, int layer, e0_expert_cache c) {
+    __shared__ SlotPlan P;
+    __shared__ uint32_t prot[E0_MAX_E / 32];
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x >= 32) return;
+    if (lane == 0) slot_plan(table, occupant, n_slots, E, next, n_next, nullptr, 0, &P, prot);
+    __syncwarp();
+    int32_t* plan = c.scratch;
+    uint32_t clock = c.counters[0];
+    int n = 0;
+    for (int i = 0; i < P.n; ++i) {
+        const int key = layer * E + P.e[i];
+        int src = -1, fill = -1;
+        const int hit = (key >= 0 && key < c.n_keys) ? c.map[key] : -1;
+        if (hit >= 0 && hit < c.capacity) {
+            src = hit;
+            if (lane == 0) {
+                c.stamp[hit] = ++clock;
+                c.counters[1] += 1;
+            }
+        } else {
+            if (lane == 0) c.counters[2] += 1;
+            if (c.capacity > 0 && key >= 0 && key < c.n_keys) {
+                // least recently used entry (an empty one first: stamp 0), the
+                // warp scanning a strided share each, ties to the lower entry
+                uint32_t best = 0xffffffffu;
+                int bi = 0x7fffffff;
+                for (int j = lane; j < c.capacity; j += 32)
+                    if (c.stamp[j] < best) {
+                        best = c.stamp[j];
+                        bi = j;
+                    }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    const uint32_t ob = __shfl_xor_sync(0xffffffffu, best, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                    if (ob < best || (ob == best && oi < bi)) {
+                        best = ob;
+                        bi = oi;
+                    }
+                }
+                fill = bi;
+                if (lane == 0) {
+                    const int old = c.key[fill];
+                    if (old >= 0 && old < c.n_keys) {
+                        c.map[old] = -1;
+                        c.counters[3] += 1;
+                    }
+                    c.key[fill] = key;
+                    c.map[key] = fill;
+                    c.stamp[fill] = ++clock;
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) {
+            plan[4 + 4 * n + 0] = P.e[i];
+            plan[4 + 4 * n + 1] = P.s[i];
+            plan[4 + 4 * n + 2] = src;
+            plan[4 + 4 * n + 3] = fill;
+        }
+        ++n;
+        __syncwarp();  // lane 0's bookkeeping is seen by every lane's next scan
+    }
+    if (lane == 0) {
+        plan[0] = n;
+        c.counters[0] = clock;
+    }
+}
+
+__global__ void k_cache_copy(uint8_t* pool, const uint8_t* bank, e0_expert_cache c, size_t sbytes) {
+    const int32_t* plan = c.scratch;
+    const int n = plan[0];
+    const size_t chunks = sbytes / 16;
+    const size_t total = chunks * (size_t)n;
+    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (size_t)gridDim.x * blockDim.x) {
+        const int i = (int)(q / chunks);
+        const size_t off = (q % chunks) * 16;
+        const int e = plan[4 + 4 * i], s = plan[4 + 4 * i + 1], src = plan[4 + 4 * i + 2], fill = plan[4 + 4 * i + 3];
+        const uint8_t* from = src >= 0 ? c.data + (size_t)src * sbytes : bank + (size_t)e * sbytes;
+        const uint4 v = *reinterpret_cast<const uint4*>(from + off);
+        *reinterpret_cast<uint4*>(pool + (size_t)s * sbytes + off) = v;
+        if (fill >= 0) *reinterpret_cast<uint4*>(c.data + (size_t)fill * sbytes + off) = v;
+    }
+}
+
 // ================================================================== routing / norm
 
 __global__ void k_route(const float* logits, int T, int E, RouteP rp, int32_t* inds, float* w, uint32_t* st) {
@@ -1063,6 +1156,19 @@ int stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* 
     if (layer < 0 || layer >= hdr.L || t_next < 1) return E0_ERR_ARG;
     const int32_t* next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
     return slot_update(pool, next, hdr.K, nullptr, 0, bank, st, s);
+}
+
+int stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot_pool* p, const uint8_t* bank,
+                                  const e0_expert_cache* c, uint32_t* st, cudaStream_t s) {
+    StackHdr hdr;
+    if (!stack_hdr(ws, &hdr)) return E0_ERR_ARG;
+    if (layer < 0 || layer >= hdr.L || t_next < 1) return E0_ERR_ARG;
+    if ((long)(layer + 1) * p->E > c->n_keys) return E0_ERR_ARG;
+    const int32_t* next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
+    k_cache_plan<<<1, 32, 0, s>>>(p->slot_table, p->occupant, p->n_slots, p->E, next, hdr.K, layer, *c);
+    k_cache_copy<<<num_sms(), 512, 0, s>>>(p->data, bank, *c, slot_bytes(p->H, p->I));
+    k_slot_commit<<<1, 32, 0, s>>>(p->slot_table, p->occupant, p->n_slots, p->E, next, hdr.K, nullptr, 0, st);
+    return launch_ok();
 }
 
 int stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* trace, int impl, uint32_t* st,

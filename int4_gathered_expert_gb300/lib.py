@@ -52,6 +52,11 @@ class Prerouter(C.Structure):
                 ("H", i32), ("E", i32), ("hidden", i32)]
 
 
+class ExpertCache(C.Structure):
+    _fields_ = [("data", C.c_void_p), ("key", C.c_void_p), ("stamp", C.c_void_p), ("map", C.c_void_p),
+                ("counters", C.c_void_p), ("scratch", C.c_void_p), ("capacity", C.c_int32), ("n_keys", C.c_int32)]
+
+
 class StackLayer(C.Structure):
     _fields_ = [("pool", SlotPool), ("W_router", vp), ("shared", C.POINTER(SharedExpert)),
                 ("head", C.POINTER(Prerouter)), ("consumer", i32)]
@@ -96,6 +101,8 @@ def load() -> C.CDLL:
         "e0_stack_step_range": (C.c_int, [vp, vp, vp, C.c_int, C.c_int, P(StackTrace), vp, vp]),
         "e0_stack_update_layers": (C.c_int, [vp, P(StackLayer), C.c_int, vp]),
         "e0_stack_prefetch_experts": (C.c_int, [vp, C.c_int, C.c_int, P(SlotPool), vp, vp, vp]),
+        "e0_stack_prefetch_experts_cached": (C.c_int, [vp, C.c_int, C.c_int, P(SlotPool), vp, P(ExpertCache), vp,
+                                                       vp]),
         "e0_prefill_sort": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, vp, vp, vp, vp, sz, vp]),
         "e0_moe_prefill_forward": (C.c_int, [vp, C.c_int, P(SlotPool), vp, P(RouteParams), vp, vp, vp,
                                              vp, sz, vp, vp]),
@@ -117,7 +124,8 @@ def exported_symbols():
             "e0_route_sigmoid_group", "e0_rmsnorm", "e0_moe_block_forward", "e0_moe_block_forward_noalloc",
             "e0_prerouter_forward",
             "e0_stack_workspace_size", "e0_stack_prepare", "e0_stack_step", "e0_stack_step_range",
-            "e0_stack_update_layers", "e0_stack_prefetch_experts", "e0_prefill_sort",
+            "e0_stack_update_layers", "e0_stack_prefetch_experts", "e0_stack_prefetch_experts_cached",
+            "e0_prefill_sort",
             "e0_moe_prefill_forward", "e0_selftest_bounded_wait", "e0_read_status", "e0_status_string"]
 
 
@@ -265,6 +273,13 @@ def e0_stack_prefetch_experts(ws, layer, t_next, pool: SlotPool, bank, status=No
     rc = load().e0_stack_prefetch_experts(ptr(ws), int(layer), int(t_next), C.byref(pool), ptr(bank), ptr(status),
                                           stream_handle(stream))
     return _check("e0_stack_prefetch_experts", rc, raise_on_error)
+
+
+def e0_stack_prefetch_experts_cached(ws, layer, t_next, pool: SlotPool, bank, cache: ExpertCache, status=None,
+                                     stream=None, raise_on_error=True):
+    rc = load().e0_stack_prefetch_experts_cached(ptr(ws), int(layer), int(t_next), C.byref(pool), ptr(bank),
+                                                 C.byref(cache), ptr(status), stream_handle(stream))
+    return _check("e0_stack_prefetch_experts_cached", rc, raise_on_error)
 
 
 def e0_prefill_sort(inds, T, K, E, counts, offsets, perm, ws, ws_bytes, stream=None, raise_on_error=True):

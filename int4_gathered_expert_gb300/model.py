@@ -141,6 +141,28 @@ class StackDev:
         return out
 
 
+class ExpertCacheDev:
+    """A cross-layer cache of `capacity` expert bundles in device memory (keys
+    layer * E + expert), least recently used first out."""
+
+    def __init__(self, capacity: int, n_layers: int, H: int, I: int, E: int, device="cuda"):
+        self.capacity = capacity
+        sb = L.e0_slot_bytes(H, I)
+        self.data = torch.empty(max(capacity, 1) * sb, dtype=torch.uint8, device=device)
+        self.key = torch.full((max(capacity, 1),), -1, dtype=torch.int32, device=device)
+        self.stamp = torch.zeros(max(capacity, 1), dtype=torch.int32, device=device)
+        self.map = torch.full((n_layers * E,), -1, dtype=torch.int32, device=device)
+        self.counters = torch.zeros(4, dtype=torch.int32, device=device)
+        self.scratch = torch.zeros(4 + 4 * 32, dtype=torch.int32, device=device)
+        self.desc = L.ExpertCache(self.data.data_ptr(), self.key.data_ptr(), self.stamp.data_ptr(),
+                                  self.map.data_ptr(), self.counters.data_ptr(), self.scratch.data_ptr(),
+                                  capacity, n_layers * E)
+
+    def stats(self) -> dict:
+        c = self.counters.cpu().tolist()
+        return {"hits": c[1], "misses": c[2], "evictions": c[3]}
+
+
 class StreamedStack:
     """Host-tier staged streaming on top of a StackDev (cluster kernel).
 
@@ -152,11 +174,14 @@ class StreamedStack:
     layers from split on while the first half of the next token runs.  Layer
     split - 1, whose prediction is final only once the token has ended but
     which the next token's first half uses, stays in the resident bank, as do
-    the layers that route natively."""
+    the layers that route natively.  With an ExpertCacheDev the copies first
+    look in a cross-layer cache of recently used bundles in device memory."""
 
-    def __init__(self, sd: "StackDev", split: int, device="cuda"):
+    def __init__(self, sd: "StackDev", split: int, device="cuda", cache: Optional["ExpertCacheDev"] = None,
+                 host: Optional[dict] = None):
         self.sd = sd
         self.split = split
+        self.cache = cache
         consumers = [l for l in range(sd.L) if sd.layers[l].consumer]
         self.batch1 = [l for l in consumers if l <= split - 2]
         self.batch2 = [l for l in consumers if l >= split]
@@ -165,10 +190,13 @@ class StreamedStack:
         self.pools = {}
         n_slots = 2 * sd.K
         for l in self.staged:
-            src = sd.pools[l].data
-            h = torch.empty(src.shape, dtype=torch.uint8, pin_memory=True)
-            h.copy_(src)
-            self.host[l] = h
+            if host is not None and l in host:  # the pinned copies of an earlier run of the same stack
+                self.host[l] = host[l]
+            else:
+                src = sd.pools[l].data
+                h = torch.empty(src.shape, dtype=torch.uint8, pin_memory=True)
+                h.copy_(src)
+                self.host[l] = h
             self.pools[l] = SlotPoolDev(sd.H, sd.I, sd.E, n_slots, device)
         torch.cuda.synchronize()
         self.cs = torch.cuda.Stream()
@@ -183,8 +211,12 @@ class StreamedStack:
 
     def _prefetch(self, layers, t_next, stream):
         for l in layers:
-            L.e0_stack_prefetch_experts(self.sd.ws, l, t_next, self.pools[l].desc, self.host[l], self.status,
-                                        stream=stream)
+            if self.cache is not None:
+                L.e0_stack_prefetch_experts_cached(self.sd.ws, l, t_next, self.pools[l].desc, self.host[l],
+                                                   self.cache.desc, self.status, stream=stream)
+            else:
+                L.e0_stack_prefetch_experts(self.sd.ws, l, t_next, self.pools[l].desc, self.host[l], self.status,
+                                            stream=stream)
 
     def start(self, x0: torch.Tensor, out: Optional[torch.Tensor] = None):
         """Token 0 (every layer routes natively) from the resident bank, then the

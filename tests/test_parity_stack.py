@@ -209,3 +209,40 @@ def test_streamed_stack_matches_resident(L, overlap):
     for l in ss.staged:
         tab = ss.pools[l].table.cpu().numpy()
         assert 0 < (tab >= 0).sum() <= 2 * m.shape.layer.K
+
+
+@pytest.mark.parametrize("capacity", [3, 64])
+def test_streamed_stack_with_expert_cache(L, capacity):
+    """Staged streaming with a cross-layer LRU cache of expert bundles in front
+    of the host bank: transparent (same tokens as the resident run), and the
+    counters add up (every copy is a hit or a miss; a cache smaller than the
+    working set evicts)."""
+    from int4_gathered_expert_gb300.model import ExpertCacheDev, StackDev, StreamedStack
+    m = _tiny_stream_model()
+    ref = StackDev(m, trace=True)
+    want = run_stack(ref, m, 6, impl=0)
+    sd = StackDev(m, trace=True)
+    cache = ExpertCacheDev(capacity, sd.L, sd.H, sd.I, sd.E)
+    ss = StreamedStack(sd, split=5, cache=cache)
+    X = torch.from_numpy(m.x).cuda()
+    copies = 0
+    occ = None
+    ss.start(X[0])
+    got = [{k: v.cpu().numpy().copy() for k, v in sd.tr.items()}]
+    occ = {l: ss.pools[l].occupant.cpu().numpy().copy() for l in ss.staged}
+    copies += sum(int((o >= 0).sum()) for o in occ.values())
+    for t in range(1, 6):
+        ss.step(X[t])
+        torch.cuda.synchronize()
+        got.append({k: v.cpu().numpy().copy() for k, v in sd.tr.items()})
+        for l in ss.staged:
+            now = ss.pools[l].occupant.cpu().numpy()
+            copies += int((now != occ[l]).sum())
+            occ[l] = now.copy()
+    assert L.e0_read_status(sd.status) == 0
+    for t in range(6):
+        assert rel_l2(got[t]["r"], want[t]["r"]) < 1e-4, t
+    st = cache.stats()
+    assert st["hits"] + st["misses"] == copies
+    if capacity < 5 * 4:
+        assert st["evictions"] > 0
