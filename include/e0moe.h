@@ -298,8 +298,11 @@ size_t e0_stack_workspace_size(int L, int H, int I, int E, int K, int head_hidde
  * history (the next step is token 0).  Synchronises the stream.  Also sizes
  * the cluster kernel (impl 2): its teams and the shared-memory regions that
  * hold each layer's weight slices; slices that do not fit are read from
- * global memory.  The environment variable E0MOE_STAGE_LIMIT (bytes), when
- * set, lowers that shared-memory budget (a test hook for the global path). */
+ * global memory.  By default a block holds the gate/up slices in full and
+ * the down slices as far as it stays within 128 KB, which leaves the rest of
+ * the SM's shared-memory/L1 array to L1.  The environment variable
+ * E0MOE_STAGE_LIMIT (bytes), when set, replaces that budget (at most the
+ * device's opt-in maximum; a test hook for full and partial staging). */
 int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
                      const e0_route_params* rp, void* ws, size_t ws_bytes, e0_stream_t stream);
 

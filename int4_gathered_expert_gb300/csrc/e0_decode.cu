@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 
@@ -984,14 +985,14 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
         // teams: as many 8-CTA clusters as can be resident at once with the
         // largest shared-memory footprint; every team must hold at most
         // T2_MAX_UNITS half-groups of a layer
-        size_t limit = smem_optin();
-        // E0MOE_STAGE_LIMIT (bytes) caps the block's shared memory, so that the
-        // weight slices that no longer fit are read from global memory (a test
-        // hook for that path)
-        if (const char* env = getenv("E0MOE_STAGE_LIMIT")) {
-            const long v = atol(env);
-            if (v > 0 && (size_t)v < limit) limit = (size_t)v;
-        }
+        const size_t optin = smem_optin();
+        size_t limit = optin;
+        // E0MOE_STAGE_LIMIT (bytes) sets the block's shared-memory budget in
+        // place of the default below (at most the opt-in maximum), so that the
+        // tests can run the staging fully, partly or hardly at all
+        long env_limit = 0;
+        if (const char* env = getenv("E0MOE_STAGE_LIMIT")) env_limit = atol(env);
+        if (env_limit > 0 && (size_t)env_limit < limit) limit = (size_t)env_limit;
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3((num_sms() / TEAM) * TEAM);
@@ -1033,6 +1034,13 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
         gu = (gu + 127) & ~(size_t)127;
         dn = (dn + 127) & ~(size_t)127;
         const size_t base = T2Smem(H, E, L, rp->K, 0, 0).total;
+        // Default budget: the gate/up slices in full, the down slices only as
+        // far as the block stays within T2_SMEM_BUDGET.  Shared memory and L1
+        // share one array per SM: a block of at most 128 KB leaves about
+        // 124 KB to L1, which caches the kernel's local-memory traffic and the
+        // slices read from global memory.  On GB300 this measured ~10 % faster
+        // per token than taking the full opt-in maximum for staging.
+        if (env_limit <= 0) limit = std::min(optin, std::max(T2_SMEM_BUDGET, base + gu));
         // two down regions; the down side gives way first, then the gate/up side
         if (base + gu + 2 * dn > limit) dn = base + gu < limit ? (((limit - base - gu) / 2) & ~(size_t)127) : 0;
         if (base + gu + 2 * dn > limit) gu = base < limit ? ((limit - base) & ~(size_t)127) : 0;

@@ -79,17 +79,20 @@ E0_DEV void cl_st(uint32_t addr, float v) {
 E0_DEV void grid_barrier2(StackHdr* S, unsigned long long target, uint32_t* st) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
+        // the block barrier above orders every thread's writes before this
+        // release, which makes them visible to whoever acquires the count
         asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(&S->bar_ctr), "l"(1ull) : "memory");
         uint32_t it = 0;
         while (true) {
             unsigned long long v;
             asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(v) : "l"(&S->bar_ctr) : "memory");
             if (v >= target) break;
-            unsigned ab;
-            asm volatile("ld.relaxed.gpu.u32 %0, [%1];" : "=r"(ab) : "l"(&S->bar_abort) : "memory");
-            if (ab) break;
-            if (++it > (1u << 24)) {
+            if ((++it & 63u) == 0) {  // the abort flag is polled less often
+                unsigned ab;
+                asm volatile("ld.relaxed.gpu.u32 %0, [%1];" : "=r"(ab) : "l"(&S->bar_abort) : "memory");
+                if (ab) break;
+            }
+            if (it > (1u << 24)) {
                 set_status(st, E0_ST_TIMEOUT);
                 atomicExch(&S->bar_abort, 1u);
                 break;
@@ -255,7 +258,9 @@ E0_DEV void hrow_dot_gelu4(const __half* w, size_t ld, int nrows, const float* h
 
 // ------------------------------------------------------------------ staging of weight slices
 
-constexpr int T2_EXPERT_W = 8;   // warps 0..7: experts; 8..11: prerouter heads and staging
+constexpr int T2_EXPERT_W = 8;
+constexpr int T2_RES_BATCH = 4;  // residual groups a warp loads at once
+constexpr size_t T2_SMEM_BUDGET = 128 * 1024;  // default shared memory of a block   // warps 0..7: experts; 8..11: prerouter heads and staging
 constexpr int T2_GU_BATCH = 2;  // gate/up rows a warp loads before it computes
 constexpr int T2_MAX_SEG = 4;    // gate/up row runs of one member (one per expert touched)
 
@@ -801,19 +806,31 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
         {
             const float* ysrc = l == 0 ? x : S.y_acc + (size_t)((l - 1) % 3) * H;
             float ss = 0.f;
-            for (int g = warp; g < GH; g += NW) {
-                const int j = GROUP * g + 2 * lane;
-                const float2 y2 = __ldcg(reinterpret_cast<const float2*>(ysrc + j));
-                float2 v = y2;
-                if (l > 0) {
-                    const float2 r2 = *reinterpret_cast<const float2*>(r + j);
-                    v = make_float2(r2.x + y2.x, r2.y + y2.y);
+            // a warp's groups (up to T2_RES_BATCH at a time) are loaded together,
+            // so their L2 reads overlap, then updated and quantised
+            for (int g0 = warp; g0 < GH; g0 += T2_RES_BATCH * NW) {
+                float2 v[T2_RES_BATCH];
+#pragma unroll
+                for (int q = 0; q < T2_RES_BATCH; ++q) {
+                    const int g = g0 + q * NW;
+                    if (g < GH) v[q] = __ldcg(reinterpret_cast<const float2*>(ysrc + GROUP * g + 2 * lane));
                 }
-                *reinterpret_cast<float2*>(r + j) = v;
-                ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
-                // word k of group g sits at hpl[k * GH + g]: lanes that read
-                // consecutive groups touch consecutive 16-byte words
-                quantize_group_v(v, hpl + g, hxg + g, lane, nullptr, GH);
+#pragma unroll
+                for (int q = 0; q < T2_RES_BATCH; ++q) {
+                    const int g = g0 + q * NW;
+                    if (g < GH) {
+                        const int j = GROUP * g + 2 * lane;
+                        if (l > 0) {
+                            const float2 r2 = *reinterpret_cast<const float2*>(r + j);
+                            v[q] = make_float2(r2.x + v[q].x, r2.y + v[q].y);
+                        }
+                        *reinterpret_cast<float2*>(r + j) = v[q];
+                        ss = fmaf(v[q].x, v[q].x, fmaf(v[q].y, v[q].y, ss));
+                        // word k of group g sits at hpl[k * GH + g]: lanes that read
+                        // consecutive groups touch consecutive 16-byte words
+                        quantize_group_v(v[q], hpl + g, hxg + g, lane, nullptr, GH);
+                    }
+                }
             }
             ss = warp_sum(ss);
             if (lane == 0) red[warp] = ss;

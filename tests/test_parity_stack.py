@@ -154,11 +154,12 @@ def test_tiny_stack_cluster_kernel(L):
     check_stack(m, traces, (0, 1, 2, 3))
 
 
-@pytest.mark.parametrize("limit", [120000, 96000])
+@pytest.mark.parametrize("limit", [1 << 20, 120000, 96000])
 def test_35b_cluster_kernel_partial_staging(L, stack35, limit, monkeypatch):
-    """With the shared-memory budget lowered, some (120 KB: the down slices) or
-    most (96 KB: part of the gate/up rows too) weight slices are read from
-    global memory instead of the staging regions; results must not change."""
+    """The shared-memory budget set by hand: the opt-in maximum (every slice
+    staged, down slices double-buffered), 120 KB (the down slices read from
+    global memory) or 96 KB (part of the gate/up rows too); results must not
+    change."""
     m, sd = stack35
     a = run_stack(sd, m, 3, impl=0)
     monkeypatch.setenv("E0MOE_STAGE_LIMIT", str(limit))
