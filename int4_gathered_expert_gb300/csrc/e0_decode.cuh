@@ -63,13 +63,27 @@ struct DecodeArgs {
 
 // ------------------------------------------------------------------ routing
 
+// A float (not NaN) as an unsigned integer of the same order; -0 and +0 map
+// alike.  0 is the key of no number (its inverse is a NaN pattern), so it
+// stays free for "no candidate".
+E0_DEV uint32_t float_order_key(float x) {
+    uint32_t u = __float_as_uint(x);
+    if ((u << 1) == 0) u = 0;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+E0_DEV float float_of_order_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // One warp routes one token.  Ranking uses the fp32 logits (softmax and
 // sigmoid are monotonic), ties go to the lower expert id, output is in
 // descending score order.  scr: E floats of per-warp shared scratch.
 template <int MAXM>
 E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds, float* w, float* scr,
                          uint32_t* st, int lane) {
-    float v[MAXM];
+    // scores are held as order keys (see float_order_key): ranking needs
+    // only their order, and the winners' values are decoded from the keys
+    uint32_t key[MAXM];
     bool bad = false;
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) {
@@ -82,7 +96,7 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
                 x = -INFINITY;
             }
         }
-        v[m] = x;
+        key[m] = float_order_key(x);
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(st, E0_ST_NONFINITE);
     uint32_t alive = 0;
@@ -95,7 +109,7 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
             const int e = lane + 32 * m;
-            if (e < E) scr[e] = sigmoid_f(v[m]);
+            if (e < E) scr[e] = sigmoid_f(float_of_order_key(key[m]));
         }
         __syncwarp();
         float gscore = -INFINITY;
@@ -140,36 +154,27 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
         }
     }
 
+    // Each round takes the largest live score with two warp reductions: the
+    // largest order key (a float's order as an unsigned integer, 0 for "no
+    // candidate"), then the lowest expert id holding it.
     int my_ind = -1;
     float my_val = 0.f;
     for (int k = 0; k < rp.K; ++k) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        bool have = false;
+        uint32_t bk = 0;
+        uint32_t bi = 0xffffffffu;
 #pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-            if ((alive >> m) & 1u) {
-                if (!have || v[m] > bv) {
-                    bv = v[m];
-                    bi = lane + 32 * m;
-                    have = true;
-                }
+        for (int m = 0; m < MAXM; ++m)
+            if (((alive >> m) & 1u) && key[m] > bk) {  // strict: the lower id wins a tie
+                bk = key[m];
+                bi = (uint32_t)(lane + 32 * m);
             }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (bi == 0x7fffffff) break;  // fewer candidates than K (validated away on the host)
-        if ((bi & 31) == lane) alive &= ~(1u << (bi >> 5));
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        if (mk == 0) break;  // fewer candidates than K (validated away on the host)
+        const uint32_t wi = __reduce_min_sync(0xffffffffu, bk == mk ? bi : 0xffffffffu);
+        if ((int)(wi & 31) == lane) alive &= ~(1u << (wi >> 5));
         if (lane == k) {
-            my_ind = bi;
-            my_val = bv;
+            my_ind = (int)wi;
+            my_val = float_of_order_key(mk);
         }
     }
     float wk;

@@ -53,6 +53,32 @@ def test_softmax_topk(L, T, E, K):
     assert L.e0_read_status(st) == 0
 
 
+def test_softmax_topk_signed_zero_and_extremes(L):
+    """Ranking compares scores as floats: -0 and +0 tie (lower id first), the
+    smallest subnormal ranks above zero, and the largest finite magnitudes
+    keep their order."""
+    E, K = 64, 6
+    logits = np.full((3, E), -1.0, np.float32)
+    logits[0, [9, 3, 5]] = [0.0, 0.0, -0.0]                      # three-way tie at zero
+    logits[1, [7, 2]] = [30.0, -3.0e38]                          # far apart
+    logits[1, 11] = np.float32(1.0e-45)                          # smallest subnormal beats -0
+    logits[1, 12] = -0.0
+    logits[2, :] = -3.0e38
+    logits[2, [40, 20]] = [-2.9e38, -2.9e38]
+    inds = torch.empty((3, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((3, K), dtype=torch.float32, device="cuda")
+    st = status_word()
+    L.e0_route_softmax_topk(dev(logits), 3, E, K, inds, w, st)
+    got = inds.cpu().numpy()
+    assert list(got[0, :3]) == [3, 5, 9]
+    assert list(got[1, :3]) == [7, 11, 12]
+    assert list(got[2, :2]) == [20, 40]
+    rt = O.route_softmax_topk(logits.astype(np.float64), K)
+    ex, msgs = routing_matches(got, w.cpu().numpy(), rt, allow_tie=False)
+    assert not msgs, msgs[:5]
+    assert L.e0_read_status(st) == 0
+
+
 @pytest.mark.parametrize("T,E,n,G,K,s", [(40, 128, 8, 4, 8, 2.5), (16, 8, 4, 2, 2, 2.5), (8, 64, 1, 1, 6, 1.0),
                                           (8, 64, 8, 8, 4, 1.5), (7, 256, 32, 3, 5, 2.0)])
 def test_sigmoid_group(L, T, E, n, G, K, s):
