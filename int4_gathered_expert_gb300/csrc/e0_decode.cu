@@ -297,6 +297,7 @@ struct StackHdr {
     float* zres2;        // [2][E] head linear-residual outputs
     float* z2;           // [2][E] head logits
     int32_t grid2, smem2, teams, smem2_gu, smem2_dn;
+    int32_t split_heavy;  // team split: cost of a LoRA-carrying shared unit (routed unit = 2)
 };
 
 struct TraceP {
@@ -1011,6 +1012,13 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
             ncl = 0;
         }
         int teams = num_sms() / TEAM;
+        // E0MOE_SPLIT_HEAVY overrides the cost of a LoRA-carrying shared unit
+        // in the team split (a tuning hook; 2 = a routed unit's cost)
+        hdr.split_heavy = T2_SPLIT_HEAVY;
+        if (const char* env = getenv("E0MOE_SPLIT_HEAVY")) {
+            const int v = atoi(env);
+            if (v >= 2 && v <= 64) hdr.split_heavy = v;
+        }
         if (ncl < teams) teams = ncl;
         // the largest run of half-group units a team takes, over the layer
         // configurations of this stack
@@ -1020,7 +1028,7 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
             const bool heavy = sh && layers[l].shared->A_gate != nullptr;
             if (heavy && layers[l].shared->rank > rank) rank = layers[l].shared->rank;
             for (int tau = 0; tau < teams; ++tau) {
-                const T2Split sp(I, rp->K, sh, heavy, tau, teams);
+                const T2Split sp(I, rp->K, sh, heavy, hdr.split_heavy, tau, teams);
                 if (sp.u1 - sp.u0 > max_units) max_units = sp.u1 - sp.u0;
             }
         }

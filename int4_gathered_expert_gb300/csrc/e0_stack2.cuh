@@ -260,7 +260,8 @@ E0_DEV void hrow_dot_gelu4(const __half* w, size_t ld, int nrows, const float* h
 
 constexpr int T2_EXPERT_W = 8;
 constexpr int T2_RES_BATCH = 4;  // residual groups a warp loads at once
-constexpr size_t T2_SMEM_BUDGET = 128 * 1024;  // default shared memory of a block   // warps 0..7: experts; 8..11: prerouter heads and staging
+constexpr size_t T2_SMEM_BUDGET = 128 * 1024;  // default shared memory of a block
+constexpr int T2_SPLIT_HEAVY = 4;  // cost of a LoRA-carrying shared unit in the split (routed = 2)   // warps 0..7: experts; 8..11: prerouter heads and staging
 constexpr int T2_GU_BATCH = 2;  // gate/up rows a warp loads before it computes
 constexpr int T2_MAX_SEG = 4;    // gate/up row runs of one member (one per expert touched)
 
@@ -328,6 +329,11 @@ E0_DEV void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
                      (uint32_t)__cvta_generic_to_shared(dst)),
                  "l"(src), "r"(bytes), "r"((uint32_t)__cvta_generic_to_shared(bar))
                  : "memory");
+}
+// Bulk prefetch of a global range into L2 (16-byte aligned, size a multiple
+// of 16); a hint with nothing to wait for.
+E0_DEV void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 E0_DEV void mbar_init2(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(bar)), "r"(count)
@@ -427,8 +433,12 @@ E0_DEV void stage_issue(const StageTab* tab, const uint8_t* const* slots, int K,
             }
             const uint8_t* b = reinterpret_cast<const uint8_t*>(bv);
             const uint8_t* p = b ? b + e.off : nullptr;
-            const bool cp = p && e.soff >= 0 && !(reinterpret_cast<uintptr_t>(p) & 15u);
+            const bool al = p && !(reinterpret_cast<uintptr_t>(p) & 15u);
+            const bool cp = al && e.soff >= 0;
             rec[i] = cp ? buf + e.soff : p;
+            // a range left in global memory is brought into L2 now, so that its
+            // reads later in the layer hit L2 instead of HBM
+            if (al && !cp && e.bytes > 0 && !(e.bytes & 15u)) prefetch_l2(p, e.bytes);
             if (cp) {
                 from[r] = p;
                 to[r] = e.soff;
@@ -552,7 +562,7 @@ __host__ __device__ inline void stage_need(int H, int I, int units, int rank, si
 // ------------------------------------------------------------------ shared memory layout
 
 struct T2Smem {
-    size_t hdr, lyr, r, hpl, hxg, ateam, apl, axg, zred, zg, zu, zd, inds, w, slots, scr, red, hnext, plan, bars, stage_gu,
+    uint32_t hdr, lyr, r, hpl, hxg, ateam, apl, axg, zred, zg, zu, zd, inds, w, slots, scr, red, hnext, plan, bars, stage_gu,
         stage_dn, dn_bytes, total;
     __host__ __device__ T2Smem(int H, int E, int L, int K, size_t gu_cap, size_t dn_cap) {
         const int GH = H / GROUP;
@@ -621,19 +631,21 @@ struct T2Smem {
 // fewer units.
 struct T2Split {
     int HG, NU, u0, u1, rows;
-    __host__ __device__ static int bound(int HG, int KH, int NU, bool heavy, int tau, int NT) {
+    // wh: cost of a shared-expert unit that carries LoRA, in halves of a
+    // routed unit's cost
+    __host__ __device__ static int bound(int HG, int KH, int NU, bool heavy, int wh, int tau, int NT) {
         if (!heavy) return (int)((long)tau * NU / NT);
-        const long Wt = 2L * KH + 4L * (NU - KH);  // cost in half units
+        const long Wt = 2L * KH + (long)wh * (NU - KH);  // cost in half units
         const long w = (long)tau * Wt / NT;
-        return w <= 2L * KH ? (int)(w / 2) : KH + (int)((w - 2L * KH) / 4);
+        return w <= 2L * KH ? (int)(w / 2) : KH + (int)((w - 2L * KH) / wh);
     }
     // nk_r routed experts; sh: a shared expert follows; heavy: it carries LoRA
-    __host__ __device__ T2Split(int I, int nk_r, bool sh, bool heavy, int tau, int NT) {
+    __host__ __device__ T2Split(int I, int nk_r, bool sh, bool heavy, int wh, int tau, int NT) {
         HG = I / 32;
         const int KH = nk_r * HG;
         NU = KH + (sh ? HG : 0);
-        u0 = bound(HG, KH, NU, sh && heavy, tau, NT);
-        u1 = bound(HG, KH, NU, sh && heavy, tau + 1, NT);
+        u0 = bound(HG, KH, NU, sh && heavy, wh, tau, NT);
+        u1 = bound(HG, KH, NU, sh && heavy, wh, tau + 1, NT);
         rows = (u1 - u0) * 32;
     }
 };
@@ -722,7 +734,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 
     auto split_of = [&](int l) {
         const LayerP& Lq = lyr[l];
-        return T2Split(I, K, Lq.sh != nullptr, Lq.sh != nullptr && Lq.Ag != nullptr, team, NT);
+        return T2Split(I, K, Lq.sh != nullptr, Lq.sh != nullptr && Lq.Ag != nullptr, S.split_heavy, team, NT);
     };
     // Staging.  The gate/up region holds one layer at a time and completes once
     // per layer (layer l waits on parity (l - lb) & 1, counting from the first
