@@ -258,10 +258,10 @@ E0_DEV void hrow_dot_gelu4(const __half* w, size_t ld, int nrows, const float* h
 
 // ------------------------------------------------------------------ staging of weight slices
 
-constexpr int T2_EXPERT_W = 8;
+constexpr int T2_EXPERT_W = 8;   // warps 0..7: experts; 8..11: prerouter heads and staging
 constexpr int T2_RES_BATCH = 4;  // residual groups a warp loads at once
 constexpr size_t T2_SMEM_BUDGET = 128 * 1024;  // default shared memory of a block
-constexpr int T2_SPLIT_HEAVY = 4;  // cost of a LoRA-carrying shared unit in the split (routed = 2)   // warps 0..7: experts; 8..11: prerouter heads and staging
+constexpr int T2_SPLIT_HEAVY = 5;  // cost of a LoRA-carrying shared unit in the split (routed = 2)
 constexpr int T2_GU_BATCH = 2;  // gate/up rows a warp loads before it computes
 constexpr int T2_MAX_SEG = 4;    // gate/up row runs of one member (one per expert touched)
 
@@ -626,9 +626,9 @@ struct T2Smem {
 // Work split of one layer: NU half-group units (the nk_r routed experts
 // first, then the shared expert when there is one), cut into NT contiguous
 // runs of about equal cost; team tau takes units [u0, u1).  A unit of a shared
-// expert with LoRA costs twice a routed one (its team also computes the LoRA
-// A and B products and waits for one more team exchange), so such teams get
-// fewer units.
+// expert with LoRA costs 2.5 times a routed one by default (its team also
+// computes the LoRA A and B products and waits for one more team exchange;
+// 2.5 measured faster than 2 or 3 on GB300), so such teams get fewer units.
 struct T2Split {
     int HG, NU, u0, u1, rows;
     // wh: cost of a shared-expert unit that carries LoRA, in halves of a
@@ -1069,6 +1069,14 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             cl_arrive();
             // the next layer's down side goes to the other down region now
             if (warp == HW && next_known) stage_dn_for(l + 1);
+            // a next layer that routes natively: the router rows this block will
+            // compute are brought into L2 now
+            if (warp == HW + 2 && lane == 0 && l + 1 < le && layer_native(S, lyr[l + 1], t)) {
+                const int e0 = b * NW, ne = min(NW, E - e0);
+                const __half* wr = lyr[l + 1].W_r + (size_t)e0 * H;
+                if (ne > 0 && !(reinterpret_cast<uintptr_t>(wr) & 15u) && !((H * 2) & 15))
+                    prefetch_l2(wr, (uint32_t)ne * H * 2);
+            }
             // one warp of the last block (not the issuing one) routes owner l-2's logits
             if (b == nb - 1 && warp == HW + 1 && l >= 2 && lyr[l - 2].fc1)
                 stack_route_head(S, l - 2, t, scr, tr, st, lane, S.z2 + (size_t)((l - 1) & 1) * E);
