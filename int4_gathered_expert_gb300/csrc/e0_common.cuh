@@ -48,16 +48,23 @@ E0_DEV float seg_sum(float v, int G, int lane) {
 
 // ---------------------------------------------------------------- loads
 
-E0_DEV uint4 ldg_stream(const void* p) {  // weights: read once, do not keep in L1
+// L2 policy for data read once (streamed weights): first out when L2 needs
+// room, so that the streamed bytes do not push out what is read again.
+E0_DEV uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+E0_DEV uint4 ldg_stream(const void* p) {  // weights: read once, kept neither in L1 nor long in L2
     uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+                 : "l"(p), "l"(l2_evict_first()));
     return v;
 }
 E0_DEV uint32_t ldg_u32(const void* p) {
     uint32_t v;
-    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(l2_evict_first()));
     return v;
 }
 

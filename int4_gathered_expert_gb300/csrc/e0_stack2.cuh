@@ -324,11 +324,13 @@ struct StagePlan {
 };
 
 E0_DEV void fence_async_smem2() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// weight slices are read once from HBM: evict-first in L2
 E0_DEV void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     (uint32_t)__cvta_generic_to_shared(dst)),
-                 "l"(src), "r"(bytes), "r"((uint32_t)__cvta_generic_to_shared(bar))
-                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            (uint32_t)__cvta_generic_to_shared(dst)),
+        "l"(src), "r"(bytes), "r"((uint32_t)__cvta_generic_to_shared(bar)), "l"(l2_evict_first())
+        : "memory");
 }
 // Bulk prefetch of a global range into L2 (16-byte aligned, size a multiple
 // of 16); a hint with nothing to wait for.
