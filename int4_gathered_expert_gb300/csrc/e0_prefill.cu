@@ -592,6 +592,53 @@ static size_t gemm2_smem() { return (size_t)P2_STAGES * P2_STAGE + 1024 + 256; }
 
 // ------------------------------------------------------------------ small prefill kernels
 
+// Smallest gap between consecutive scores among the K+1 largest of one
+// token's (biased) logits, one warp: K+1 rounds of two warp reductions over
+// order keys (the same ranking as the routing itself).
+template <int MAXM>
+__device__ float topk_gap_t(const float* lg, int E, const float* bias, int K, int lane) {
+    uint32_t key[MAXM];
+    uint32_t alive = 0;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        const int e = lane + 32 * m;
+        key[m] = 0;
+        if (e < E) {
+            float x = __ldcg(lg + e) + (bias ? bias[e] : 0.f);
+            if (!isfinite(x)) x = -INFINITY;
+            key[m] = float_order_key(x);
+            alive |= 1u << m;
+        }
+    }
+    float prev = 0.f, mingap = INFINITY;
+    for (int k = 0; k <= K && k < E; ++k) {
+        uint32_t bk = 0, bi = 0xffffffffu;
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m)
+            if (((alive >> m) & 1u) && key[m] > bk) {
+                bk = key[m];
+                bi = (uint32_t)(lane + 32 * m);
+            }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        if (mk == 0) break;
+        const uint32_t wi = __reduce_min_sync(0xffffffffu, bk == mk ? bi : 0xffffffffu);
+        if ((int)(wi & 31) == lane) alive &= ~(1u << (wi >> 5));
+        const float v = float_of_order_key(mk);
+        if (k > 0) mingap = fminf(mingap, prev - v);
+        prev = v;
+    }
+    return mingap;
+}
+
+__device__ float topk_gap(const float* lg, int E, const float* bias, int K, int lane) {
+    if (E <= 32) return topk_gap_t<1>(lg, E, bias, K, lane);
+    if (E <= 64) return topk_gap_t<2>(lg, E, bias, K, lane);
+    if (E <= 128) return topk_gap_t<4>(lg, E, bias, K, lane);
+    if (E <= 256) return topk_gap_t<8>(lg, E, bias, K, lane);
+    if (E <= 512) return topk_gap_t<16>(lg, E, bias, K, lane);
+    return topk_gap_t<32>(lg, E, bias, K, lane);
+}
+
 // Route one token per warp from the tensor-core logits; flag tokens whose
 // top-(K+1) logits (plus bias) have a gap below REFINE_GAP.
 __global__ void k_prefill_route(const float* logits, int T, int E, RouteP rp, int32_t* inds, float* w,
@@ -602,38 +649,11 @@ __global__ void k_prefill_route(const float* logits, int T, int E, RouteP rp, in
     if (t >= T) return;
     const float* lg = logits + (size_t)t * E;
     route_warp(lg, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr + warp * E, st, lane);
-    // smallest gap among the K+1 largest (biased) logits
-    float prev = INFINITY, mingap = INFINITY;
-    uint32_t taken[32];
-    const int MAXM = (E + 31) / 32;
-    for (int m = 0; m < 32; ++m) taken[m] = 0;
-    for (int k = 0; k <= rp.K && k < E; ++k) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int m = 0; m < MAXM; ++m) {
-            const int e = lane + 32 * m;
-            if (e < E && !taken[m]) {
-                const float v = lg[e] + (rp.logit_bias ? rp.logit_bias[e] : 0.f);
-                if (bi == 0x7fffffff || v > bv) {
-                    bv = v;
-                    bi = e;
-                }
-            }
-        }
-        for (int o = 16; o; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (bi == 0x7fffffff) break;
-        if ((bi & 31) == lane) taken[bi >> 5] = 1;
-        if (k > 0) mingap = fminf(mingap, prev - bv);
-        prev = bv;
-    }
-    if (lane == 0 && (rp.mode != E0_ROUTE_SOFTMAX_TOPK || mingap < REFINE_GAP)) flag[1 + atomicAdd(flag, 1)] = t;
+    // softmax routing is refined where two of the K+1 largest scores are close;
+    // sigmoid-group routing always is
+    const bool refine =
+        rp.mode != E0_ROUTE_SOFTMAX_TOPK || topk_gap(lg, E, rp.logit_bias, rp.K, lane) < REFINE_GAP;
+    if (lane == 0 && refine) flag[1 + atomicAdd(flag, 1)] = t;
 }
 
 // fp16 row slice (64 halves) . fp16 x slice (64 halves), fp32 accumulation
