@@ -262,7 +262,9 @@ constexpr int T2_EXPERT_W = 8;   // warps 0..7: experts; 8..11: prerouter heads 
 constexpr int T2_RES_BATCH = 4;  // residual groups a warp loads at once
 constexpr size_t T2_SMEM_BUDGET = 128 * 1024;  // default shared memory of a block
 constexpr int T2_SPLIT_HEAVY = 5;  // cost of a LoRA-carrying shared unit in the split (routed = 2)
-constexpr int T2_GU_BATCH = 2;  // gate/up rows a warp loads before it computes
+// gate/up rows a warp loads before it computes: one row keeps the fewest
+// values live (spills cost more here than the longer chain of rows)
+constexpr int T2_GU_BATCH = 1;
 constexpr int T2_MAX_SEG = 4;    // gate/up row runs of one member (one per expert touched)
 
 constexpr int T2_STAGE_RANK = 16;   // LoRA ranks up to this are staged; larger ones read global memory
