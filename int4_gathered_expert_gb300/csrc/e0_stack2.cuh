@@ -170,19 +170,20 @@ E0_DEV float h8_dot44(const uint4 wv, const float4 a, const float4 b) {
 // This lane's part of an fp16 row (n halves, n a multiple of 8) times an fp32
 // vector in shared memory: the lane takes 8 consecutive elements out of every
 // 256, so one load of the warp covers 512 contiguous bytes of the row and the
-// shared-memory reads of neighbouring lanes do not collide.  Sum the lanes
-// with warp_sum.
+// shared-memory reads of neighbouring lanes do not collide.  Four such loads
+// are in flight at a time: more would raise the kernel's register peak, and
+// its spills cost more than the extra round trip.  Sum the lanes with warp_sum.
 E0_DEV float hrow_dot(const __half* w, const float* x, int n, int lane) {
     float acc = 0.f;
-    for (int c0 = 0; c0 < n; c0 += 8 * 256) {
-        uint4 wv[8];
+    for (int c0 = 0; c0 < n; c0 += 4 * 256) {
+        uint4 wv[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
             const int c = c0 + k * 256 + lane * 8;
             if (c < n) wv[k] = ldg_stream(w + c);
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
             const int c = c0 + k * 256 + lane * 8;
             if (c < n)
                 acc += h8_dot44(wv[k], *reinterpret_cast<const float4*>(x + c), *reinterpret_cast<const float4*>(x + c + 4));
@@ -1033,15 +1034,16 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             }
             asm volatile("bar.sync 1, %0;" ::"r"(T2_EXPERT_W * 32));
             // ---- down rows: lane = output row, partial over the team's columns
+            // (four half-group units in flight: the register peak, as above)
             for (int jr = warp * 32 + lane; jr - lane < rows_m; jr += T2_EXPERT_W * 32) {
                 if (jr >= rows_m) continue;
                 const int j = j0 + jr;
                 float acc = 0.f;
-                for (int ub = sp.u0; ub < sp.u1; ub += 8) {
-                    uint4 cv[8];
-                    uint32_t sbv[8];
+                for (int ub = sp.u0; ub < sp.u1; ub += 4) {
+                    uint4 cv[4];
+                    uint32_t sbv[4];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < 4; ++q) {
                         const int u = ub + q;
                         if (u < sp.u1 && plan.dn_codes(db, u - sp.u0) && plan.dn_sb(db, u - sp.u0)) {
                             cv[q] = *reinterpret_cast<const uint4*>(plan.dn_codes(db, u - sp.u0) + (size_t)jr * 16);
@@ -1049,7 +1051,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
                         }
                     }
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < 4; ++q) {
                         const int u = ub + q;
                         if (u >= sp.u1 || !plan.dn_codes(db, u - sp.u0) || !plan.dn_sb(db, u - sp.u0)) continue;
                         const int ke = u / sp.HG;
