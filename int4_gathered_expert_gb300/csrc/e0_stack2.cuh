@@ -223,15 +223,17 @@ __device__ __noinline__ float hrow_dot_gelu(const __half* w, const float* hp, in
 
 // Up to four consecutive fp16 rows (row stride ld halves) of the head's second
 // layer times gelu_erf(hp), hp written by other blocks earlier in the launch
-// (read from L2); the activation is evaluated once for all rows.
+// (read from L2); the activation is evaluated once for all rows.  One chunk
+// of 256 columns at a time: this is off the layer's critical path, and more
+// loads in flight here set the kernel's register peak.
 E0_DEV void hrow_dot_gelu4(const __half* w, size_t ld, int nrows, const float* hp, int n, int lane,
                                             float* acc) {
     float s[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < n; c0 += 2 * 256) {
-        uint4 wv[4][2];
-        float4 a[2], b[2];
+    for (int c0 = 0; c0 < n; c0 += 256) {
+        uint4 wv[4][1];
+        float4 a[1], b[1];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < 1; ++k) {
             const int c = c0 + k * 256 + lane * 8;
             if (c < n) {
                 a[k] = __ldcg(reinterpret_cast<const float4*>(hp + c));
@@ -242,7 +244,7 @@ E0_DEV void hrow_dot_gelu4(const __half* w, size_t ld, int nrows, const float* h
             }
         }
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < 1; ++k) {
             const int c = c0 + k * 256 + lane * 8;
             if (c < n) {
                 const float4 ga = make_float4(gelu_erf_f(a[k].x), gelu_erf_f(a[k].y), gelu_erf_f(a[k].z), gelu_erf_f(a[k].w));
