@@ -302,7 +302,11 @@ size_t e0_stack_workspace_size(int L, int H, int I, int E, int K, int head_hidde
  * the down slices as far as it stays within 128 KB, which leaves the rest of
  * the SM's shared-memory/L1 array to L1.  The environment variable
  * E0MOE_STAGE_LIMIT (bytes), when set, replaces that budget (at most the
- * device's opt-in maximum; a test hook for full and partial staging). */
+ * device's opt-in maximum; a test hook for full and partial staging).
+ * E0MOE_SPLIT_HEAVY (2..64, default 5) sets the cost of a shared-expert unit
+ * that carries LoRA in the split of a layer's units over the teams, in
+ * halves of a routed unit's cost (a tuning hook; out-of-range values are
+ * ignored). */
 int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
                      const e0_route_params* rp, void* ws, size_t ws_bytes, e0_stream_t stream);
 
