@@ -78,3 +78,33 @@ def test_host_validation_codes(lib):
     assert lib.e0_stack_step(None, None, None, None, 0, None, None) == L.E0_ERR_NULL
     assert lib.e0_stack_step(C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), None, 0, None, None) == L.E0_ERR_ARG
     assert lib.e0_status_string(L.E0_ERR_CUDA).decode().startswith("CUDA")
+
+
+def test_host_validation_of_ranges_prefetch_and_selftest(lib):
+    """Layer ranges, the host-tier prefetch (plain and through the expert
+    cache), layer updates and the bounded-wait self-test reject null
+    pointers, workspaces that no stack was prepared in, and out-of-range
+    waits on the host, before any launch."""
+    from int4_gathered_expert_gb300 import lib as L
+    unknown = C.c_void_p(256)   # never passed to e0_stack_prepare
+    some = C.c_void_p(512)
+    assert lib.e0_stack_step_range(None, None, None, 0, 1, None, None, None) == L.E0_ERR_NULL
+    assert lib.e0_stack_step_range(some, some, unknown, 0, 1, None, None, None) == L.E0_ERR_ARG
+    layer = L.StackLayer()
+    assert lib.e0_stack_update_layers(None, C.byref(layer), 1, None) == L.E0_ERR_NULL
+    assert lib.e0_stack_update_layers(unknown, None, 1, None) == L.E0_ERR_NULL
+    assert lib.e0_stack_update_layers(unknown, C.byref(layer), 1, None) == L.E0_ERR_ARG
+    pool = L.SlotPool(16, 16, 16, 8, 2048, 512, 256)
+    assert lib.e0_stack_prefetch_experts(None, 7, 1, C.byref(pool), some, None, None) == L.E0_ERR_NULL
+    assert lib.e0_stack_prefetch_experts(unknown, 7, 1, None, some, None, None) == L.E0_ERR_NULL
+    assert lib.e0_stack_prefetch_experts(unknown, 7, 1, C.byref(pool), None, None, None) == L.E0_ERR_NULL
+    assert lib.e0_stack_prefetch_experts(unknown, 7, 1, C.byref(pool), some, None, None) == L.E0_ERR_ARG
+    cache = L.ExpertCache(16, 16, 16, 16, 16, 16, 64, 40 * 256)
+    assert lib.e0_stack_prefetch_experts_cached(unknown, 7, 1, C.byref(pool), some, None, None,
+                                                None) == L.E0_ERR_NULL
+    assert lib.e0_stack_prefetch_experts_cached(unknown, 7, 1, C.byref(pool), some, C.byref(cache), None,
+                                                None) == L.E0_ERR_ARG
+    assert lib.e0_selftest_bounded_wait(None, 1000, some, None) == L.E0_ERR_NULL
+    assert lib.e0_selftest_bounded_wait(some, 1000, None, None) == L.E0_ERR_NULL
+    assert lib.e0_selftest_bounded_wait(some, 0, some, None) == L.E0_ERR_ARG
+    assert lib.e0_selftest_bounded_wait(some, L.E0_SELFTEST_MAX_WAIT_US + 1, some, None) == L.E0_ERR_ARG
