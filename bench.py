@@ -53,8 +53,8 @@ def parse():
     p.add_argument("--tokens-per-step", type=int, default=256)
     p.add_argument("--no-cpu", action="store_true", help="skip the timed CPU-oracle baseline")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--kernel-impl", type=int, default=2,
-                   help="2 cluster kernel (default), 0 persistent cooperative kernel, 1 per-phase chain")
+    p.add_argument("--kernel-impl", type=int, default=3,
+                   help="3 flag-carrying-word kernel (default), 0 persistent cooperative kernel, 1 per-phase chain")
     p.add_argument("--layers", type=int, default=40, help="fewer layers: a small case for profiling only")
     p.add_argument("--no-prefill", action="store_true", help="skip the whole-layer prefill measurement")
     p.add_argument("--prefill-only", action="store_true")
@@ -375,8 +375,8 @@ def whole_job_rate(units_per_rank: int, world: int, seconds_max: float) -> float
 
 
 # launches of this library's kernels per decode token, by stack implementation
-LAUNCHES_PER_TOKEN = {0: 1, 2: 1}
-KERNEL_NAME = {0: "k_stack_token", 1: "k_stack_gateup/k_stack_down chain", 2: "k_stack_token2"}
+LAUNCHES_PER_TOKEN = {0: 1, 3: 1}
+KERNEL_NAME = {0: "k_stack_token", 1: "k_stack_gateup/k_stack_down chain", 3: "k_stack_ll"}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -552,7 +552,7 @@ def run_gb300(args):
                          "through the 40-layer stack, float64 numpy oracle"}
 
     streaming = None
-    if rank == 0 and not args.no_streaming and args.kernel_impl == 2:
+    if rank == 0 and not args.no_streaming and args.kernel_impl == 3:
         del sd
         torch.cuda.empty_cache()
         try:
@@ -582,7 +582,8 @@ def run_gb300(args):
                                  % (nb["total"] / 1e6),
                            "kernel": {0: "persistent cooperative kernel, one launch per token",
                                       1: "per-phase kernel chain",
-                                      2: "cluster kernel (8-CTA teams), one launch per token"}.get(args.kernel_impl)},
+                                      3: "flag-carrying-word kernel (one CTA per SM, no grid barrier), one "
+                                         "launch per token"}.get(args.kernel_impl)},
                 "expert_weight_gbs": value * nb["routed"] / 1e9 / ws if ws else None,
                 "weight_gbs": value * nb["total"] / 1e9 / ws if ws else None,
                 "bytes_per_token": nb,

@@ -46,13 +46,16 @@
  * e0_slot_bytes(H, I) bytes:
  *     [0, I*H)                 gate/up codes, row-interleaved: for each i the
  *                              gate row i (H/2 bytes) then the up row i
- *     [I*H, I*H + H*I/2)       down codes, half-group major: the 16 bytes of
- *                              row j, inputs 32c..32c+31, at (c*H + j)*16
+ *     [I*H, I*H + H*I/2)       down codes in blocks of 16 output rows: the
+ *                              16 bytes of row j, inputs 32c..32c+31, at
+ *                              ((j/16 * I/32 + c) * 16 + j%16) * 16
  *     next I*(H/64)*2*4 bytes  gate/up (scale, bias) fp16 pairs, [I][2][H/64]
- *     next H*(I/64)*4 bytes    down (scale, bias) fp16 pairs, group major:
- *                              group g of row j at (g*H + j)*4
- * (A down slice "rows j0..j1 of half-group c" is one contiguous range, so it
- * can be fetched with one bulk copy.)  Inside every 32-bit word (8
+ *     next H*(I/64)*4 bytes    down (scale, bias) fp16 pairs in the same
+ *                              row blocks: group g of row j at
+ *                              ((j/16 * I/64 + g) * 16 + j%16) * 4
+ * (Every input of a block of 16 output rows is one contiguous range of codes
+ * and one of (scale, bias) words, so a decode block's share of the down
+ * projection is two bulk copies per expert.)  Inside every 32-bit word (8
  * elements e0..e7 of a row) the nibbles are interleaved: nibble j (bits
  * 4j..4j+3, little-endian word) holds e0, e2, e4, e6, e1, e3, e5, e7 for
  * j = 0..7.  Masking a word with 0x000F000F / 0x00F000F0 (and the same after
@@ -87,7 +90,9 @@ enum {
     E0_ST_BAD_EXPERT = 2u,   /* an expert id outside [0, E): ignored        */
     E0_ST_NONFINITE = 4u,    /* a routing score was NaN or infinite         */
     E0_ST_TIMEOUT = 8u,      /* a bounded device-side wait gave up          */
-    E0_ST_POOL_FULL = 16u    /* slot_update found no free slot              */
+    E0_ST_POOL_FULL = 16u,   /* slot_update found no free slot              */
+    E0_ST_INTERNAL = 32u     /* a kernel's own consistency check failed; the
+                                step was skipped (results are not valid)    */
 };
 
 /* ---- routing rules -------------------------------------------------- */
@@ -295,18 +300,13 @@ typedef struct e0_stack_trace {
 size_t e0_stack_workspace_size(int L, int H, int I, int E, int K, int head_hidden);
 
 /* Copy the layer descriptors into the workspace and clear the routing
- * history (the next step is token 0).  Synchronises the stream.  Also sizes
- * the cluster kernel (impl 2): its teams and the shared-memory regions that
- * hold each layer's weight slices; slices that do not fit are read from
- * global memory.  By default a block holds the gate/up slices in full and
- * the down slices as far as it stays within 128 KB, which leaves the rest of
- * the SM's shared-memory/L1 array to L1.  The environment variable
- * E0MOE_STAGE_LIMIT (bytes), when set, replaces that budget (at most the
- * device's opt-in maximum; a test hook for full and partial staging).
- * E0MOE_SPLIT_HEAVY (2..64, default 5) sets the cost of a shared-expert unit
- * that carries LoRA in the split of a layer's units over the teams, in
- * halves of a routed unit's cost (a tuning hook; out-of-range values are
- * ignored). */
+ * history and the flag-carrying words (the next step is token 0).
+ * Synchronises the stream.  Also sizes the flag-carrying-word kernel (impl 3):
+ * one block of 17 warps per SM and the shared memory that stages each
+ * layer's weight slices.  Environment (read here): E0MOE_WAIT_US (1..10^7,
+ * default 200000) is the longest a device-side wait of impl 3 polls before
+ * it gives up with E0_ST_TIMEOUT; E0MOE_PF_DIST (0..64, default 0) makes
+ * impl 3 also prefetch the weights of that many layers ahead into L2. */
 int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
                      const e0_route_params* rp, void* ws, size_t ws_bytes, e0_stream_t stream);
 
@@ -317,19 +317,25 @@ int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
  *   0 = one persistent cooperative kernel per token, two or three grid
  *       barriers per layer (deterministic);
  *   1 = a chain of per-phase kernels (deterministic, equal to 0 bit for bit);
- *   2 = one cooperative launch of 8-CTA thread-block clusters per token, one
- *       grid barrier per layer: each cluster computes a slice of the layer's
- *       experts end to end, exchanging activations through distributed
- *       shared memory, and adds its partial outputs with atomic adds (the
- *       summation order, and so the last bits, may vary between runs).
- *       E0_ERR_UNSUPPORTED when no cluster configuration fits the device. */
+ *   2 = retired: returns E0_ERR_UNSUPPORTED;
+ *   3 = one cooperative launch per token of the flag-carrying-word kernel:
+ *       blocks exchange the layer's activations and residual rows through
+ *       64-bit (epoch, value) words instead of grid barriers, and stage every
+ *       weight slice with bulk copies issued a layer ahead where the routing
+ *       is known (deterministic; sums in another order than 0).  Built for
+ *       the layer shapes (H, I, E, K) = (2048, 512, 256, 2 / 4 / 8),
+ *       (1536, 384, 128, 8), (256, 128, 16, 4) with LoRA ranks 8 or 16;
+ *       other stacks -> E0_ERR_UNSUPPORTED (use 0).  A device-side wait that
+ *       gives up sets E0_ST_TIMEOUT in d_status and a flag in the workspace
+ *       that makes every later impl-3 step of it give up at once: prepare
+ *       the stack again after a timeout. */
 int e0_stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* trace,
                   int impl, uint32_t* d_status, e0_stream_t stream);
 
 /* ---- staged streaming of predicted experts ------------------------------ */
 
-/* Layers [layer_begin, layer_end) of the current token with the cluster
- * kernel (impl 2).  A token is the launches whose ranges cover 0..L in order
+/* Layers [layer_begin, layer_end) of the current token with the
+ * flag-carrying-word kernel (impl 3).  A token is the launches whose ranges cover 0..L in order
  * on one stream; x is read by the range that starts at 0, r_out written by
  * the range that ends at L (the token counter advances there).  Between the
  * launches of a token the caller may run other work on other streams, e.g.
@@ -337,7 +343,7 @@ int e0_stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* 
  * is already final.  ([KOALA] §1-§2, [JAEHUN] §3.1: the prediction made one
  * token ahead is what lets the load of the next token's experts overlap the
  * current token.)  Errors: unknown workspace or empty / out-of-range layer
- * range -> E0_ERR_ARG; no cluster geometry -> E0_ERR_UNSUPPORTED. */
+ * range -> E0_ERR_ARG; a stack impl 3 is not built for -> E0_ERR_UNSUPPORTED. */
 int e0_stack_step_range(const float* x, float* r_out, void* ws, int layer_begin, int layer_end,
                         const e0_stack_trace* trace, uint32_t* d_status, e0_stream_t stream);
 

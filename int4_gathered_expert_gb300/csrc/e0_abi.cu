@@ -205,7 +205,7 @@ int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, c
 int e0_stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* trace, int impl, uint32_t* d_status,
                   e0_stream_t stream) {
     if (!x || !r_out || !ws) return E0_ERR_NULL;
-    if (impl < 0 || impl > 2) return E0_ERR_ARG;
+    if (impl < 0 || impl > 3) return E0_ERR_ARG;
     if (!e0::stack_known(ws)) return E0_ERR_ARG;
     return e0::stack_step(x, r_out, ws, trace, impl, d_status, cs(stream));
 }

@@ -174,6 +174,55 @@ E0_DEV float q4_group_dot(const uint4 c0, const uint4 c1, const uint4* pl, XGrou
     return xg.c * fmaf(s, (float)sqx, b * xg.sx);
 }
 
+// ---------------------------------------------------------------- 32-element half-groups
+
+// One warp quantises 32 values (one per lane; lanes beyond n hold 0) into
+// the planes of a half-group (4 uint4, kernel nibble order) and its XGroup.
+E0_DEV void quantize_half_warp(float v, uint4* planes, XGroup* xg, int lane) {
+    const float mx = warp_max(fabsf(v));
+    const float inv = (mx > 0.f && mx < 3.0e38f) ? 32767.f / mx : 0.f;
+    int q = __float2int_rn(v * inv);
+    q = max(-32767, min(32767, q));
+    const int s = warp_sum_int(q);
+    const int e = lane & 7;  // element within its 8-element word
+    const int set = (e >> 1) & 1, byte = ((e & 1) << 1) | (e >> 2);
+    const uint32_t hi = ((uint32_t)(q >> 8) & 0xFFu) << (8 * byte);
+    const uint32_t lo = ((uint32_t)q & 0xFFu) << (8 * byte);
+    uint32_t hiA = set ? 0u : hi, hiB = set ? hi : 0u, loA = set ? 0u : lo, loB = set ? lo : 0u;
+#pragma unroll
+    for (int o = 1; o <= 4; o <<= 1) {
+        hiA |= __shfl_xor_sync(0xffffffffu, hiA, o);
+        hiB |= __shfl_xor_sync(0xffffffffu, hiB, o);
+        loA |= __shfl_xor_sync(0xffffffffu, loA, o);
+        loB |= __shfl_xor_sync(0xffffffffu, loB, o);
+    }
+    if (e == 0) planes[lane >> 3] = make_uint4(hiA, hiB, loA, loB);
+    if (lane == 0) {
+        xg->c = (inv > 0.f) ? mx / 32767.f : 0.f;
+        xg->sx = (float)s;
+    }
+}
+
+// Dot product of one half-group of an int4 row (16 code bytes) with its planes.
+E0_DEV float q4_half_dot(const uint4 c, const uint4* pl, XGroup xg, uint32_t sb_bits) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    int hi = 0;
+    uint32_t lo = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 p = pl[k];
+        const uint32_t a = w[k] & 0x0F0F0F0Fu;
+        const uint32_t b = (w[k] >> 4) & 0x0F0F0F0Fu;
+        hi = dp4a_us(a, p.x, hi);
+        hi = dp4a_us(b, p.y, hi);
+        lo = dp4a_uu(a, p.z, lo);
+        lo = dp4a_uu(b, p.w, lo);
+    }
+    const int sqx = hi * 256 + (int)lo;
+    __half2 sb = *reinterpret_cast<const __half2*>(&sb_bits);
+    return xg.c * fmaf(__low2float(sb), (float)sqx, __high2float(sb) * xg.sx);
+}
+
 // fp16 weights x fp32 activations, 8 halves per uint4.
 E0_DEV float h8_dot(const uint4 wv, const float* x) {
     const __half2* h = reinterpret_cast<const __half2*>(&wv);
@@ -185,6 +234,21 @@ E0_DEV float h8_dot(const uint4 wv, const float* x) {
         acc = fmaf(f.y, x[2 * i + 1], acc);
     }
     return acc;
+}
+
+// fp16 weights x fp32 activations: 8 halves of wv times a (first 4) and b (last 4).
+E0_DEV float h8_dot44(const uint4 wv, const float4 a, const float4 b) {
+    const __half2* hw = reinterpret_cast<const __half2*>(&wv);
+    const float2 w0 = __half22float2(hw[0]), w1 = __half22float2(hw[1]);
+    const float2 w2 = __half22float2(hw[2]), w3 = __half22float2(hw[3]);
+    float acc = w0.x * a.x;
+    acc = fmaf(w0.y, a.y, acc);
+    acc = fmaf(w1.x, a.z, acc);
+    acc = fmaf(w1.y, a.w, acc);
+    acc = fmaf(w2.x, b.x, acc);
+    acc = fmaf(w2.y, b.y, acc);
+    acc = fmaf(w3.x, b.z, acc);
+    return fmaf(w3.y, b.w, acc);
 }
 
 E0_DEV float silu_f(float x) { return x / (1.f + expf(-x)); }
@@ -205,6 +269,10 @@ E0_DEV uint4 interleave16(uint4 v) {
     return make_uint4(interleave_word(v.x), interleave_word(v.y), interleave_word(v.z), interleave_word(v.w));
 }
 
+// Rows of a down block: the down projection is stored in blocks of DROWS
+// output rows, each block holding every input of its rows.
+constexpr int DROWS = 16;
+
 // Offsets inside one expert slot (the kernel layout documented in e0moe.h).
 struct SlotLayout {
     int H, I;
@@ -212,6 +280,18 @@ struct SlotLayout {
     __host__ __device__ size_t gu_sb() const { return (size_t)I * H + (size_t)H * I / 2; }
     __host__ __device__ size_t down_sb() const { return gu_sb() + (size_t)I * (H / GROUP) * 2 * 4; }
     __host__ __device__ size_t bytes() const { return down_sb() + (size_t)H * (I / GROUP) * 4; }
+    // down codes: the 16 bytes of output row j, half-group c (inputs 32c..32c+31),
+    // in row blocks: block j / DROWS holds [half-group][row in block][16 bytes]
+    __host__ __device__ size_t down_code_off(int j, int c) const {
+        return down_codes() + (((size_t)(j / DROWS) * (I / 32) + c) * DROWS + j % DROWS) * 16;
+    }
+    // down (scale, bias) word of output row j, 64-group g: [block][group][row in block]
+    __host__ __device__ size_t down_sb_off(int j, int g) const {
+        return down_sb() + (((size_t)(j / DROWS) * (I / GROUP) + g) * DROWS + j % DROWS) * 4;
+    }
+    // one row block's down codes / words are contiguous
+    __host__ __device__ size_t down_block_code_bytes() const { return (size_t)(I / 32) * DROWS * 16; }
+    __host__ __device__ size_t down_block_sb_bytes() const { return (size_t)(I / GROUP) * DROWS * 4; }
 };
 
 }  // namespace e0

@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <map>
 #include <mutex>
+#include <vector>
 
 #include "e0_decode.cuh"
 #include "e0_internal.h"
@@ -36,9 +37,9 @@ __global__ void k_pack_expert(e0_expert_q src, uint8_t* dst, int H, int I, int32
             const uint8_t* s = c < half ? src.gate.codes + i * (H / 2) + c * 16 : src.up.codes + i * (H / 2) + (c - half) * 16;
             *reinterpret_cast<uint4*>(dst + i * H + c * 16) = interleave16(*reinterpret_cast<const uint4*>(s));
         } else if (q < n_gu + n_dn) {
-            // half-group major: chunk (c, j) = row j, inputs 32c..32c+31
+            // chunk (j, c) = row j, inputs 32c..32c+31, at its row-block offset
             const size_t q2 = q - n_gu, c = q2 / H, j = q2 % H;
-            *reinterpret_cast<uint4*>(dst + sl.down_codes() + q2 * 16) =
+            *reinterpret_cast<uint4*>(dst + sl.down_code_off((int)j, (int)c)) =
                 interleave16(*reinterpret_cast<const uint4*>(src.down.codes + j * (I / 2) + c * 16));
         } else if (q < n_gu + n_dn + n_gsb) {
             const size_t p = q - n_gu - n_dn;
@@ -47,10 +48,10 @@ __global__ void k_pack_expert(e0_expert_q src, uint8_t* dst, int H, int I, int32
             const uint32_t v = (uint32_t)qt.scale[i * GH + g] | ((uint32_t)qt.bias[i * GH + g] << 16);
             *reinterpret_cast<uint32_t*>(dst + sl.gu_sb() + p * 4) = v;
         } else {
-            // group major: word (g, j) = group g of row j
+            // word (j, g) = group g of row j, at its row-block offset
             const size_t p = q - n_gu - n_dn - n_gsb, g = p / H, j = p % H;
             const uint32_t v = (uint32_t)src.down.scale[j * GI + g] | ((uint32_t)src.down.bias[j * GI + g] << 16);
-            *reinterpret_cast<uint32_t*>(dst + sl.down_sb() + p * 4) = v;
+            *reinterpret_cast<uint32_t*>(dst + sl.down_sb_off((int)j, (int)g)) = v;
         }
     }
     if (blockIdx.x == 0 && threadIdx.x == 0 && table != nullptr && eid >= 0) {
@@ -289,15 +290,18 @@ struct StackHdr {
     float* z;            // [E]
     int32_t grid;        // blocks of the persistent kernel
     int32_t smem;        // its dynamic shared memory
-    // one-barrier-per-layer cluster kernel
-    unsigned long long bar_ctr;   // monotonic arrival counter
-    unsigned long long bar_base;  // its value when the next launch starts
-    float* y_acc;        // [3][H] layer outputs accumulated with red.add
-    float* hpre2;        // [2][hidden] head fc1 outputs, by layer parity
-    float* zres2;        // [2][E] head linear-residual outputs
-    float* z2;           // [2][E] head logits
-    int32_t grid2, smem2, teams, smem2_gu, smem2_dn;
-    int32_t split_heavy;  // team split: cost of a LoRA-carrying shared unit (routed unit = 2)
+    // flag-carrying-word kernel (k_stack_ll): 64-bit (epoch << 32 | fp32) words
+    unsigned long long* llR;   // [H] residual stream after each layer
+    unsigned long long* llA;   // [(K + 2) I + 2 * 16] a-values, shared pre-activations, LoRA z_g / z_u
+    unsigned long long* llLg;  // [E] router logits of a native layer
+    unsigned long long* llHp;  // [2][hidden + E] head fc1 outputs and linear-residual outputs, by layer parity
+    unsigned long long* llZ;   // [L][E] head logits of each owner
+    unsigned long long* llZg;  // [2 * 16] LoRA z_g, z_u of the shared expert
+    unsigned long long* llZd;  // [64][16] partial sums of LoRA z_d, one row per CTA holding shared rows
+    size_t ll_bytes;           // bytes of the five buffers (cleared by e0_stack_prepare)
+    uint32_t ll_abort;         // set when a CTA gave up waiting
+    unsigned long long ll_wait_ns;  // a poll gives up after this much device time
+    int32_t grid3, smem3, pf_dist, ll_ok;
 };
 
 struct TraceP {
@@ -339,15 +343,23 @@ static size_t stack_layout(StackHdr* hdr, char* base, int L, int H, int I, int E
     float* hp = c.take<float>(hidden > 0 ? hidden : 1);
     float* zr = c.take<float>(E);
     float* z = c.take<float>(E);
-    float* yacc = c.take<float>((size_t)3 * H);
-    float* hp2 = c.take<float>((size_t)2 * (hidden > 0 ? hidden : 1));
-    float* zr2 = c.take<float>((size_t)2 * E);
-    float* z2 = c.take<float>((size_t)2 * E);
+    const size_t ll0 = (c.off + 255) & ~(size_t)255;
+    unsigned long long* llR = c.take<unsigned long long>(H);
+    unsigned long long* llA = c.take<unsigned long long>((size_t)(K + 2) * I + 32);
+    unsigned long long* llLg = c.take<unsigned long long>(E);
+    unsigned long long* llHp = c.take<unsigned long long>((size_t)2 * ((hidden > 0 ? hidden : 1) + E));
+    unsigned long long* llZ = c.take<unsigned long long>((size_t)L * E);
+    unsigned long long* llZg = c.take<unsigned long long>(2 * 16);
+    unsigned long long* llZd = c.take<unsigned long long>((size_t)64 * 16);
     if (hdr) {
-        hdr->y_acc = yacc;
-        hdr->hpre2 = hp2;
-        hdr->zres2 = zr2;
-        hdr->z2 = z2;
+        hdr->llZg = llZg;
+        hdr->llZd = llZd;
+        hdr->llR = llR;
+        hdr->llA = llA;
+        hdr->llLg = llLg;
+        hdr->llHp = llHp;
+        hdr->llZ = llZ;
+        hdr->ll_bytes = c.off - ll0;
         hdr->layers = layers;
         hdr->hist = hist;
         hdr->wcur = wcur;
@@ -635,7 +647,25 @@ __global__ void __launch_bounds__(PHASE_THREADS) k_stack_token(StackHdr* Sp, con
     }
 }
 
-#include "e0_stack2.cuh"
+#include "e0_stack_ll.cuh"
+
+// Layer shapes the flag-carrying-word kernel is built for (other shapes: impl 0).
+using LLS35K4 = LLShape<2048, 512, 256, 4>;
+using LLS35K2 = LLShape<2048, 512, 256, 2>;
+using LLS35K8 = LLShape<2048, 512, 256, 8>;
+using LLS8B = LLShape<1536, 384, 128, 8>;
+using LLSTiny = LLShape<256, 128, 16, 4>;
+
+static const void* ll_kernel(int H, int I, int E, int K) {
+    if (H == 2048 && I == 512 && E == 256) {
+        if (K == 4) return (const void*)k_stack_ll<LLS35K4>;
+        if (K == 2) return (const void*)k_stack_ll<LLS35K2>;
+        if (K == 8) return (const void*)k_stack_ll<LLS35K8>;
+    }
+    if (H == 1536 && I == 384 && E == 128 && K == 8) return (const void*)k_stack_ll<LLS8B>;
+    if (H == 256 && I == 128 && E == 16 && K == 4) return (const void*)k_stack_ll<LLSTiny>;
+    return nullptr;
+}
 
 // ================================================================== host side
 
@@ -655,10 +685,12 @@ static void init_attrs() {
     cudaFuncSetAttribute(k_stack_token, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (g_smem_optin <= 0) g_smem_optin = big;
-    cudaFuncSetAttribute(k_stack_token2, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
+    for (const void* f : {(const void*)k_stack_ll<LLS35K4>, (const void*)k_stack_ll<LLS35K2>,
+                          (const void*)k_stack_ll<LLS35K8>, (const void*)k_stack_ll<LLS8B>, (const void*)k_stack_ll<LLSTiny>})
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
 }
 
-// largest dynamic shared memory one block of the cluster kernel may take
+// largest dynamic shared memory one block may take
 static size_t smem_optin() {
     num_sms();
     return (size_t)g_smem_optin;
@@ -950,6 +982,66 @@ size_t stack_ws_bytes(int L, int H, int I, int E, int K, int hidden) {
 static std::mutex g_stack_mu;
 static std::map<const void*, StackHdr> g_stacks;
 
+// Geometry of the flag-carrying-word kernel: one CTA per SM, and whether every
+// layer's work split fits the kernel's per-CTA limits (ll_ok = 0: impl 3
+// returns E0_ERR_UNSUPPORTED for this stack).
+static void ll_geometry(StackHdr* hdr, const e0_stack_layer* layers, int L, int H, int I, int E, int K) {
+    const int nb = num_sms();
+    hdr->grid3 = nb;
+    hdr->pf_dist = LL_PF_DIST;
+    if (const char* env = getenv("E0MOE_PF_DIST")) {
+        const int v = atoi(env);
+        if (v >= 0 && v <= 64) hdr->pf_dist = v;
+    }
+    hdr->ll_wait_ns = LL_WAIT_NS;
+    if (const char* env = getenv("E0MOE_WAIT_US")) {
+        const long v = atol(env);
+        if (v >= 1 && v <= 10000000) hdr->ll_wait_ns = (unsigned long long)v * 1000ull;
+    }
+    int hidden = 0;
+    for (int l = 0; l < L; ++l)
+        if (layers[l].head && layers[l].head->hidden > hidden) hidden = layers[l].head->hidden;
+    const LLSmem lay(H, I, E, L, K, hidden, nb);
+    const LLGeo geo(H, I, E, K, hidden, nb);
+    hdr->smem3 = (int32_t)lay.total;
+    const void* fn = ll_kernel(H, I, E, K);
+    bool ok = fn != nullptr && (H + 2 * E) % 8 == 0 &&
+              (size_t)lay.total <= smem_optin() && geo.nr <= LL_MAXROWS && (K + 1) * I / 32 <= LL_NW * LL_MAXQ;
+    const int GH = H / GROUP, R = GH >= 32 ? 1 : 32 / GH;
+    auto cdiv = [](long a, long b) { return (int)((a + b - 1) / b); };
+    auto al16 = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
+    for (int l = 0; l < L && ok; ++l) {
+        const e0_stack_layer& ly = layers[l];
+        const bool sh = ly.shared != nullptr;
+        const bool lora = sh && ly.shared->A_gate != nullptr;
+        const int nk = K + (sh ? 1 : 0);
+        if (cdiv((long)nk * I, nb) > LL_NW * LL_MAXA * R) ok = false;
+        if (!al16(ly.pool.data) || !al16(ly.W_router) || (sh && !al16(ly.shared->data))) ok = false;
+        if (lora) {
+            const e0_shared_expert* x = ly.shared;
+            if (x->rank % 8 != 0 || x->rank > LL_RANK || nb < 2 * x->rank || cdiv((long)nk * I, nb) > 32) ok = false;
+            if (!al16(x->A_gate) || !al16(x->A_up) || !al16(x->B_gate) || !al16(x->B_up) || !al16(x->B_down)) ok = false;
+            // CTAs holding shared-expert rows
+            int s0 = 0;
+            while (s0 < nb && (int)((long)nk * I * (s0 + 1) / nb) <= K * I) ++s0;
+            if (nb - s0 > LL_MAX_SHCTA) ok = false;
+        }
+        if (ly.head && l + 1 < L) {
+            const int rows = cdiv((long)ly.head->hidden + E, nb);
+            if (ly.head->hidden % 256 != 0 || rows > LL_MAXROWS || rows * (H / 256) > LL_NW * LL_MAXB1) ok = false;
+            if (!al16(ly.head->fc1) || !al16(ly.head->lres) || !al16(ly.head->fc2)) ok = false;
+        }
+        if (l >= 1 && layers[l - 1].head && cdiv(E, nb) * (layers[l - 1].head->hidden / 256) > LL_NW) ok = false;
+        if (cdiv(E, nb) * (H / 256) > LL_MAX_RITEMS) ok = false;
+    }
+    int per_sm = 0;
+    if (ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, LL_THREADS, lay.total) != cudaSuccess) {
+        cudaGetLastError();
+        per_sm = 0;
+    }
+    hdr->ll_ok = ok && per_sm >= 1 ? 1 : 0;
+}
+
 int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, const e0_route_params* rp, void* ws,
                   cudaStream_t s) {
     num_sms();
@@ -981,82 +1073,7 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
     if (per_sm < 1) per_sm = 1;
     if (per_sm > 2) per_sm = 2;
     hdr.grid = num_sms() * per_sm;
-    // cluster kernel geometry
-    {
-        // teams: as many 8-CTA clusters as can be resident at once with the
-        // largest shared-memory footprint; every team must hold at most
-        // T2_MAX_UNITS half-groups of a layer
-        const size_t optin = smem_optin();
-        size_t limit = optin;
-        // E0MOE_STAGE_LIMIT (bytes) sets the block's shared-memory budget in
-        // place of the default below (at most the opt-in maximum), so that the
-        // tests can run the staging fully, partly or hardly at all
-        long env_limit = 0;
-        if (const char* env = getenv("E0MOE_STAGE_LIMIT")) env_limit = atol(env);
-        if (env_limit > 0 && (size_t)env_limit < limit) limit = (size_t)env_limit;
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof(cfg));
-        cfg.gridDim = dim3((num_sms() / TEAM) * TEAM);
-        cfg.blockDim = dim3(T2_THREADS);
-        cfg.dynamicSmemBytes = limit;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = TEAM;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        int ncl = 0;
-        if (cudaOccupancyMaxActiveClusters(&ncl, (void*)k_stack_token2, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            ncl = 0;
-        }
-        int teams = num_sms() / TEAM;
-        // E0MOE_SPLIT_HEAVY overrides the cost of a LoRA-carrying shared unit
-        // in the team split (a tuning hook; 2 = a routed unit's cost)
-        hdr.split_heavy = T2_SPLIT_HEAVY;
-        if (const char* env = getenv("E0MOE_SPLIT_HEAVY")) {
-            const int v = atoi(env);
-            if (v >= 2 && v <= 64) hdr.split_heavy = v;
-        }
-        if (ncl < teams) teams = ncl;
-        // the largest run of half-group units a team takes, over the layer
-        // configurations of this stack
-        int rank = 0, max_units = 0;
-        for (int l = 0; l < L && teams > 0; ++l) {
-            const bool sh = layers[l].shared != nullptr;
-            const bool heavy = sh && layers[l].shared->A_gate != nullptr;
-            if (heavy && layers[l].shared->rank > rank) rank = layers[l].shared->rank;
-            for (int tau = 0; tau < teams; ++tau) {
-                const T2Split sp(I, rp->K, sh, heavy, hdr.split_heavy, tau, teams);
-                if (sp.u1 - sp.u0 > max_units) max_units = sp.u1 - sp.u0;
-            }
-        }
-        if (teams > 0 && max_units > T2_MAX_UNITS) teams = 0;
-        hdr.teams = teams;
-        hdr.grid2 = teams * TEAM;
-        // staging regions: what one member needs per layer, as far as the
-        // shared memory allows
-        size_t gu = 0, dn = 0;
-        stage_need(H, I, max_units > 0 ? max_units : 1, rank, &gu, &dn);
-        gu = (gu + 127) & ~(size_t)127;
-        dn = (dn + 127) & ~(size_t)127;
-        const size_t base = T2Smem(H, E, L, rp->K, 0, 0).total;
-        // Default budget: the gate/up slices in full, the down slices only as
-        // far as the block stays within T2_SMEM_BUDGET.  Shared memory and L1
-        // share one array per SM: a block of at most 128 KB leaves about
-        // 124 KB to L1, which caches the kernel's local-memory traffic and the
-        // slices read from global memory.  On GB300 this measured ~10 % faster
-        // per token than taking the full opt-in maximum for staging.
-        if (env_limit <= 0) limit = std::min(optin, std::max(T2_SMEM_BUDGET, base + gu));
-        // two down regions; the down side gives way first, then the gate/up side
-        if (base + gu + 2 * dn > limit) dn = base + gu < limit ? (((limit - base - gu) / 2) & ~(size_t)127) : 0;
-        if (base + gu + 2 * dn > limit) gu = base < limit ? ((limit - base) & ~(size_t)127) : 0;
-        const T2Smem t2(H, E, L, rp->K, gu, dn);
-        hdr.smem2 = (int32_t)t2.total;
-        hdr.smem2_gu = (int32_t)gu;
-        hdr.smem2_dn = (int32_t)dn;
-    }
+    ll_geometry(&hdr, layers, L, H, I, E, rp->K);
     LayerP* hl = new LayerP[L];
     for (int l = 0; l < L; ++l)
         hl[l] = to_layer(&layers[l].pool, layers[l].W_router, layers[l].shared, layers[l].head, layers[l].consumer);
@@ -1064,7 +1081,7 @@ int stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E, cons
     if (cudaMemcpyAsync(ws, &hdr, sizeof(hdr), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(hdr.layers, hl, sizeof(LayerP) * L, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemsetAsync(hdr.hist, 0xff, sizeof(int32_t) * 2 * L * rp->K, s) != cudaSuccess ||
-        cudaMemsetAsync(hdr.y_acc, 0, sizeof(float) * 3 * H, s) != cudaSuccess ||
+        cudaMemsetAsync(hdr.llR, 0, hdr.ll_bytes, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         rc = E0_ERR_CUDA;
     delete[] hl;
@@ -1101,40 +1118,30 @@ static bool stack_hdr(const void* ws, StackHdr* out) {
     return true;
 }
 
-// Layers [lb, le) of the current token with the cluster kernel.
+// Layers [lb, le) of the current token with the flag-carrying-word kernel:
+// one cooperative launch (its CTAs wait on words the others write, so they
+// must be resident together; a launch that cannot guarantee it is an error).
+static int stack_step_ll(const float* x, float* r_out, void* ws, const StackHdr& hdr, int lb, int le,
+                         const e0_stack_trace* trace, uint32_t* st, cudaStream_t s) {
+    if (!hdr.ll_ok) return E0_ERR_UNSUPPORTED;
+    StackHdr* Sp = reinterpret_cast<StackHdr*>(ws);
+    TraceP tr = trace_of(trace);
+    void* args[] = {&Sp, (void*)&x, &r_out, &tr, &st, &lb, &le};
+    const void* fn = ll_kernel(hdr.H, hdr.I, hdr.E, hdr.K);
+    if (!fn) return E0_ERR_UNSUPPORTED;
+    return cuda_ok(cudaLaunchCooperativeKernel(fn, dim3(hdr.grid3), dim3(LL_THREADS), args, (size_t)hdr.smem3, s));
+}
+
+// Layers [lb, le) of the current token (the flag-carrying-word kernel).
 int stack_step_range(const float* x, float* r_out, void* ws, int lb, int le, const e0_stack_trace* trace, uint32_t* st,
                      cudaStream_t s) {
     num_sms();
-    StackHdr* Sp = reinterpret_cast<StackHdr*>(ws);
     StackHdr hdr;
     if (!stack_hdr(ws, &hdr)) return E0_ERR_ARG;
     if (lb < 0 || le > hdr.L || lb >= le) return E0_ERR_ARG;
     if (le == hdr.L && !r_out) return E0_ERR_NULL;
-    if (hdr.teams < 1) return E0_ERR_UNSUPPORTED;
-    const TraceP tr = trace_of(trace);
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(hdr.grid2);
-    cfg.blockDim = dim3(T2_THREADS);
-    cfg.dynamicSmemBytes = (size_t)hdr.smem2;
-    cfg.stream = s;
-    cudaLaunchAttribute at[2];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = TEAM;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeCooperative;
-    at[1].val.cooperative = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_stack_token2, Sp, x, r_out, tr, st, lb, le);
-    if (e != cudaSuccess) {
-        // co-residency of a grid that fits on the device at once without the cooperative attribute
-        cudaGetLastError();
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, k_stack_token2, Sp, x, r_out, tr, st, lb, le);
-    }
-    return cuda_ok(e);
+    if (lb == 0 && !x) return E0_ERR_NULL;
+    return stack_step_ll(x, r_out, ws, hdr, lb, le, trace, st, s);
 }
 
 // New layer descriptors for a prepared stack, keeping its routing history,
@@ -1207,7 +1214,8 @@ int stack_step(const float* x, float* r_out, void* ws, const e0_stack_trace* tra
         tr.head_logits = trace->head_logits;
         tr.pred_inds = trace->pred_inds;
     }
-    if (impl == 2) return stack_step_range(x, r_out, ws, 0, hdr.L, trace, st, s);
+    if (impl == 2) return E0_ERR_UNSUPPORTED;  // retired (the cluster kernel)
+    if (impl == 3) return stack_step_ll(x, r_out, ws, hdr, 0, hdr.L, trace, st, s);
     if (impl == 0) {
         const PersistSmem lay(hdr.H, hdr.E, hdr.K, (size_t)hdr.smem);
         void* args[] = {&Sp, (void*)&x, &r_out, &tr, &st};

@@ -495,7 +495,7 @@ E0_DEV void phase_down(const DecodeArgs& A, int blk, int nblk, char* smem) {
     const int ner = head ? (E + rh.R - 1) / rh.R : 0;
     const int n_fc2 = T * ner;
     const SlotLayout sl{H, I};
-    const size_t sbytes = sl.bytes(), dcode = sl.down_codes(), dsb = sl.down_sb();
+    const size_t sbytes = sl.bytes();
 
     for (int task = blk * nw + warp; task < n_down + n_fc2; task += nblk * nw) {
         if (task < n_down) {
@@ -507,16 +507,16 @@ E0_DEV void phase_down(const DecodeArgs& A, int blk, int nblk, char* smem) {
                     const int s = slots[t * K + k];
                     if (s < 0) continue;
                     const uint8_t* ex = A.L.pool + (size_t)s * sbytes;
-                    const uint8_t* cp = ex + dcode + ((size_t)(2 * rm.g) * H + j) * 16;
-                    const uint4 c0 = ldg_stream(cp), c1 = ldg_stream(cp + (size_t)H * 16);
-                    const uint32_t sb = ldg_u32(ex + dsb + ((size_t)rm.g * H + j) * 4);
+                    const uint8_t* cp = ex + sl.down_code_off(j, 2 * rm.g);
+                    const uint4 c0 = ldg_stream(cp), c1 = ldg_stream(cp + (size_t)DROWS * 16);
+                    const uint32_t sb = ldg_u32(ex + sl.down_sb_off(j, rm.g));
                     const int pq = (t * NE + k) * GI + rm.g;
                     acc = fmaf(wts[t * K + k], q4_group_dot(c0, c1, planes + pq * 8, xg[pq], sb), acc);
                 }
                 if (sh) {
-                    const uint8_t* cp = A.L.sh + dcode + ((size_t)(2 * rm.g) * H + j) * 16;
-                    const uint4 c0 = ldg_stream(cp), c1 = ldg_stream(cp + (size_t)H * 16);
-                    const uint32_t sb = ldg_u32(A.L.sh + dsb + ((size_t)rm.g * H + j) * 4);
+                    const uint8_t* cp = A.L.sh + sl.down_code_off(j, 2 * rm.g);
+                    const uint4 c0 = ldg_stream(cp), c1 = ldg_stream(cp + (size_t)DROWS * 16);
+                    const uint32_t sb = ldg_u32(A.L.sh + sl.down_sb_off(j, rm.g));
                     const int pq = (t * NE + NK) * GI + rm.g;
                     acc += q4_group_dot(c0, c1, planes + pq * 8, xg[pq], sb);
                 }

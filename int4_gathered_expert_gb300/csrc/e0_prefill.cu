@@ -373,6 +373,14 @@ E0_DEV void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst, int x,
         : "memory");
 }
 
+E0_DEV void tma_load_5d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y, int z, int w, int v) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
+        : "memory");
+}
+
 E0_DEV void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y, int z) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -432,10 +440,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             const uint8_t* sbp = nullptr;
             if (ex) {
                 if (MODE == MODE_GATEUP) sbp = ex + sl.gu_sb() + (size_t)wr * (p.H / GROUP) * 4;
-                else sbp = ex + sl.down_sb() + (size_t)wr * 4;  // group kk at + kk * H * 4
+                else sbp = ex + sl.down_sb_off(wr, 0);  // group kk at + kk * DROWS * 4
             }
             // (scale, bias) words of 8 K steps are loaded one chunk ahead of use
-            const size_t sstep = MODE == MODE_GATEUP ? (size_t)4 : (size_t)p.H * 4;
+            const size_t sstep = MODE == MODE_GATEUP ? (size_t)4 : (size_t)DROWS * 4;
             uint32_t sbw[8], sbn[8];
 #pragma unroll
             for (int d = 0; d < 8; ++d) sbn[d] = (ex && d < nk) ? ldg_u32(sbp + (size_t)d * sstep) : 0u;
@@ -458,11 +466,13 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                     }
                     uint8_t* st = smem + s * P2_STAGE;
                     if (ex) {
-                        // gate/up raw tile: [128 rows][32 B]; down raw tile: [2 half-groups][128 rows][16 B]
+                        // gate/up raw tile: [128 rows][32 B]; down raw tile: [8 row
+                        // blocks][2 half-groups][16 rows][16 B]
                         const uint8_t* raw = st + P2_A + P2_B;
-                        const uint4 c0 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 : raw + r * 16);
+                        const uint8_t* rd = raw + ((r / DROWS) * 2 * DROWS + r % DROWS) * 16;
+                        const uint4 c0 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 : rd);
                         const uint4 c1 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 + 16
-                                                                                              : raw + 2048 + r * 16);
+                                                                                              : rd + DROWS * 16);
                         dequant64_to_tile(c0, c1, sbw[d], st, r);
                     } else {
                         zero_row_of_tile(st, r);
@@ -535,7 +545,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                     uint8_t* st = smem + s * P2_STAGE;
                     mbar_arrive_expect_tx(&raw_full[s], P2_RAW + P2_B);
                     if (MODE == MODE_GATEUP) tma_load_3d(&tmCodes, &raw_full[s], st + P2_A + P2_B, kk * 32, it.m * 128, z);
-                    else tma_load_4d(&tmCodes, &raw_full[s], st + P2_A + P2_B, 0, it.m * 128, 2 * kk, z);
+                    else tma_load_5d(&tmCodes, &raw_full[s], st + P2_A + P2_B, 0, 0, 2 * kk, it.m * (128 / DROWS), z);
                     tma_load_2d(&tmB, &raw_full[s], st + P2_A, kk * BK, it.row0);
                 }
             }
@@ -818,18 +828,19 @@ static bool make_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uin
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D map over the down codes of every slot, half-group major: {16 bytes,
-// H rows, I/32 half-groups, slots}; one box = two half-groups (one 64-input
-// K step) of 128 rows, stored [2][128][16 B] in shared memory.
+// 5-D map over the down codes of every slot, in row blocks: {16 bytes, DROWS
+// rows of a block, I/32 half-groups, H/DROWS blocks, slots}; one box = two
+// half-groups (one 64-input K step) of 128 rows (8 blocks), stored
+// [8][2][DROWS][16 B] in shared memory.
 static bool make_down_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t slots,
                           uint64_t slot_stride) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[4] = {16, H, I / 32, slots};
-    cuuint64_t strides[3] = {16, H * 16, slot_stride};
-    cuuint32_t box[4] = {16, 128, 2, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+    cuuint64_t dims[5] = {16, DROWS, I / 32, H / DROWS, slots};
+    cuuint64_t strides[4] = {16, (cuuint64_t)DROWS * 16, (I / 32) * DROWS * 16, slot_stride};
+    cuuint32_t box[5] = {16, DROWS, 2, 128 / DROWS, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

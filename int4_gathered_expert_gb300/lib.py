@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libe0moe.so")
 
 E0_OK, E0_ERR_ARG, E0_ERR_NULL, E0_ERR_UNSUPPORTED, E0_ERR_CUDA = 0, -1, -2, -3, -4
-E0_ST_SLOT_MISS, E0_ST_BAD_EXPERT, E0_ST_NONFINITE, E0_ST_TIMEOUT, E0_ST_POOL_FULL = 1, 2, 4, 8, 16
+E0_ST_SLOT_MISS, E0_ST_BAD_EXPERT, E0_ST_NONFINITE, E0_ST_TIMEOUT, E0_ST_POOL_FULL, E0_ST_INTERNAL = 1, 2, 4, 8, 16, 32
 E0_ROUTE_SOFTMAX_TOPK, E0_ROUTE_SIGMOID_GROUP = 0, 1
 E0_MAX_E, E0_MAX_K, E0_MAX_T_DECODE, E0_MAX_LORA_RANK = 1024, 32, 64, 64
 
