@@ -28,9 +28,10 @@ def routing_matches(gpu_inds, gpu_w, rt, allow_tie=True):
     indices) with weights within W_ATOL; a token is exempt when the oracle's
     K-th and (K+1)-th scores (or its G-th and (G+1)-th group scores) differ by
     less than TIE_REL relative.  Within an exempt-free token, if two selected
-    experts are themselves tied the sets are compared instead of the order."""
+    experts are themselves tied the sets are compared instead of the order.
+    gpu_w None: indices only."""
     gpu_inds = np.asarray(gpu_inds)
-    gpu_w = np.asarray(gpu_w, np.float64)
+    gpu_w = None if gpu_w is None else np.asarray(gpu_w, np.float64)
     T, K = rt.inds.shape
     exempt, msgs = [], []
     for t in range(T):
@@ -42,6 +43,8 @@ def routing_matches(gpu_inds, gpu_w, rt, allow_tie=True):
             if not (_adjacent_tie(rt.scores[t], order, K) and set(gpu_inds[t]) == set(rt.inds[t])):
                 msgs.append(f"token {t}: gpu {list(gpu_inds[t])} oracle {list(rt.inds[t])} gap {rt.gap[t]:.3g}")
                 continue
+        if gpu_w is None:
+            continue
         want = {int(e): float(w) for e, w in zip(rt.inds[t], rt.w[t])}
         for e, w in zip(gpu_inds[t], gpu_w[t]):
             if abs(want[int(e)] - w) > W_ATOL:

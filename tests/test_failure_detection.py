@@ -92,7 +92,7 @@ def test_stack_status_clean_on_a_normal_token(L):
     L.e0_selftest_bounded_wait(flag, 1000, st)
     X = torch.from_numpy(m.x).cuda()
     for t in range(2):
-        sd.step(X[t], impl=2)
+        sd.step(X[t], impl=3)
     torch.cuda.synchronize()
     assert int(sd.status.item()) == 0
     assert L.e0_read_status(st) & L.E0_ST_TIMEOUT

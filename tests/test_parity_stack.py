@@ -2,7 +2,13 @@
 layers, sigmoid-group routing, heads owned by 7..22) against the CPU oracle,
 teacher-forced layer by layer: the oracle recomputes every checked layer from
 the GPU's residual stream and the GPU's routing, after checking that routing
-itself (native router or the head prediction made one token earlier)."""
+itself (native router or the head prediction made one token earlier).
+
+Routing must equal the oracle's exactly, except where the oracle's K-th and
+(K+1)-th scores (or G-th and (G+1)-th group scores) are closer than 1e-6
+relative; per-layer outputs must be within rel-L2 2e-3 of the oracle's."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -14,7 +20,8 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 N_TOK = 6
-CHECK = (0, 1, 5)
+CHECK = (0, 1, 2, 5)
+LL = 3  # the flag-carrying-word kernel (one launch per token)
 
 
 @pytest.fixture(scope="module")
@@ -29,12 +36,22 @@ def L():
     return lib
 
 
-def run_stack(sd, m, n_tok, impl):
+def snapshot(sd):
+    return {k: v.cpu().numpy().copy() for k, v in sd.tr.items()}
+
+
+def run_stack(sd, m, n_tok, impl, traced=None):
+    """Decode n_tok tokens; returns the trace of every token (or of the tokens
+    in `traced`, None elsewhere)."""
     sd.prepare()
     traces = []
+    full = sd.trace
     for t in range(n_tok):
+        keep = traced is None or t in traced
+        sd.trace = full if keep else None
         sd.step(torch.from_numpy(m.x[t]).cuda(), impl=impl)
-        traces.append({k: v.cpu().numpy().copy() for k, v in sd.tr.items()})
+        traces.append(snapshot(sd) if keep else None)
+    sd.trace = full
     return traces
 
 
@@ -73,45 +90,76 @@ def check_stack(m, traces, check, L_check=None):
                 z = O.prerouter(h, inds, p_inds, m.heads[l])
                 assert rel_l2(tr["head_logits"][l], z) < 1e-5, (t, l)
                 if l + 1 < nL:
-                    # the prediction's indices (its weights are checked when it is consumed)
+                    # the predicted routing: indices and weights as the oracle
+                    # routes the head logits, exempt only at ties
                     rt = O.route(z[None], ls)
-                    gi = tr["pred_inds"][l + 1]
-                    if rt.gap[0] >= 1e-6 and rt.group_gap[0] >= 1e-6:
-                        assert set(gi) == set(rt.inds[0]), (t, l, gi, rt.inds[0])
-                    else:
-                        n_exempt += 1
+                    ex, msgs = routing_matches(tr["pred_inds"][l + 1][None],
+                                               _pred_w(traces, t, l + 1, ls.K), rt)
+                    assert not msgs, (t, l, msgs)
+                    n_exempt += len(ex)
     return worst, n_exempt
+
+
+def _pred_w(traces, t, l, K):
+    """The weights of a prediction are what the consumer uses at the next token
+    (the trace records the weights each layer used); without a next-token
+    trace, the weight check is skipped (the indices are still compared)."""
+    nxt = traces[t + 1] if t + 1 < len(traces) else None
+    if nxt is not None and np.array_equal(nxt["inds"][l], traces[t]["pred_inds"][l]):
+        return nxt["w"][l][None]
+    return None
 
 
 @pytest.fixture(scope="module")
 def stack35(L):
     from int4_gathered_expert_gb300.model import StackDev
-    m = synth.stack_model(synth.STACK35B, n_tokens=N_TOK)
+    m = synth.stack_model(synth.STACK35B, n_tokens=256)
     sd = StackDev(m, trace=True)
     yield m, sd
     del sd
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("impl", [0, 2])
+@pytest.mark.parametrize("impl", [0, LL])
 def test_35b_stack_teacher_forced(L, stack35, impl):
     m, sd = stack35
     traces = run_stack(sd, m, N_TOK, impl=impl)
     assert L.e0_read_status(sd.status) == 0
-    worst, _ = check_stack(m, traces, CHECK)
-    print("35B stack impl", impl, "worst per-layer rel-L2", worst)
+    worst, n_ex = check_stack(m, traces, CHECK)
+    print("35B stack impl", impl, "worst per-layer rel-L2", worst, "tie-exempt", n_ex)
 
 
-def test_35b_cluster_kernel_agrees_with_persistent(L, stack35):
-    """impl 2 adds partial outputs with atomics, so only the last bits may
-    differ from the deterministic kernel; routing must agree except at ties."""
+def test_35b_stack_late_token(L, stack35):
+    """Token 255 of the 256-token AR(1) stream (experts recur): the state the
+    kernel carries from token to token (routing history, predictions, flag
+    epochs) still gives oracle results late in the stream."""
+    m, sd = stack35
+    traces = run_stack(sd, m, 256, impl=LL, traced={253, 254, 255})
+    assert L.e0_read_status(sd.status) == 0
+    worst, n_ex = check_stack(m, traces, (254, 255))
+    print("35B stack token 255: worst per-layer rel-L2", worst, "tie-exempt", n_ex)
+
+
+def test_35b_ll_kernel_agrees_with_persistent(L, stack35):
+    """Both kernels are deterministic; their sums are taken in different orders,
+    so the residual streams agree to rounding and the routing exactly (a routing
+    difference would have to be a tie, which the oracle check above exempts)."""
     m, sd = stack35
     a = run_stack(sd, m, 4, impl=0)
-    b = run_stack(sd, m, 4, impl=2)
+    b = run_stack(sd, m, 4, impl=LL)
     for t in range(4):
         assert rel_l2(b[t]["r"], a[t]["r"]) < 1e-4, t
-        same = (a[t]["inds"] == b[t]["inds"]).all(axis=1)
-        assert same.mean() > 0.95, (t, same.mean())
+        assert np.array_equal(a[t]["inds"], b[t]["inds"]), t
+        assert np.array_equal(a[t]["pred_inds"], b[t]["pred_inds"]), t
+
+
+def test_35b_ll_kernel_is_deterministic(L, stack35):
+    m, sd = stack35
+    a = run_stack(sd, m, 3, impl=LL)
+    b = run_stack(sd, m, 3, impl=LL)
+    for t in range(3):
+        for k in ("r", "inds", "w", "head_logits", "pred_inds"):
+            assert np.array_equal(a[t][k], b[t][k]), (t, k)
 
 
 def test_35b_stack_chain_equals_persistent(L, stack35):
@@ -134,43 +182,71 @@ def stack8(L):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("impl", [0, 2])
+@pytest.mark.parametrize("impl", [0, LL])
 def test_8b_stack_teacher_forced(L, stack8, impl):
     m, sd = stack8
     traces = run_stack(sd, m, N_TOK, impl=impl)
     assert L.e0_read_status(sd.status) == 0
-    worst, _ = check_stack(m, traces, CHECK)
-    print("8B stack impl", impl, "worst per-layer rel-L2", worst)
+    worst, n_ex = check_stack(m, traces, CHECK)
+    print("8B stack impl", impl, "worst per-layer rel-L2", worst, "tie-exempt", n_ex)
 
 
-def test_tiny_stack_cluster_kernel(L):
-    """A 5-layer tiny stack (H=256, E=16) through impl 2, teacher-forced."""
+def test_tiny_stack_ll_kernel(L):
+    """A 5-layer tiny stack (H=256, E=16: eight rows a warp) through the kernel."""
     from int4_gathered_expert_gb300.model import StackDev
     shape = synth.StackShape(layer=synth.TINY, n_layers=5, owners=(1, 2, 3), shared_expert=True, seed=13)
     m = synth.stack_model(shape, n_tokens=4, threads=2)
     sd = StackDev(m, trace=True)
-    traces = run_stack(sd, m, 4, impl=2)
+    traces = run_stack(sd, m, 4, impl=LL)
     assert L.e0_read_status(sd.status) == 0
     check_stack(m, traces, (0, 1, 2, 3))
 
 
-@pytest.mark.parametrize("limit", [1 << 20, 120000, 96000])
-def test_35b_cluster_kernel_partial_staging(L, stack35, limit, monkeypatch):
-    """The shared-memory budget set by hand: the opt-in maximum (every slice
-    staged, down slices double-buffered), 120 KB (the down slices read from
-    global memory) or 96 KB (part of the gate/up rows too); results must not
-    change."""
-    m, sd = stack35
-    a = run_stack(sd, m, 3, impl=0)
-    monkeypatch.setenv("E0MOE_STAGE_LIMIT", str(limit))
-    b = run_stack(sd, m, 3, impl=2)
-    monkeypatch.delenv("E0MOE_STAGE_LIMIT")
-    sd.prepare()
+@pytest.mark.parametrize("K,prerouter", [(2, True), (8, True), (4, False)])
+def test_35b_shape_route_k_and_prerouter_variants(L, K, prerouter):
+    """The K / prerouter arms of the harness (softmax-top-K on the 35B layer
+    shape, 8 layers): K = 2 and K = 8 with heads owned by 2..6, and K = 4 with
+    no heads (every layer routes with its own router)."""
+    from int4_gathered_expert_gb300.model import StackDev
+    shape = dataclasses.replace(synth.STACK35B, layer=dataclasses.replace(synth.L35B, K=K), n_layers=8,
+                                owners=tuple(range(2, 7)) if prerouter else (), seed=40 + K)
+    m = synth.stack_model(shape, n_tokens=4)
+    sd = StackDev(m, trace=True)
+    traces = run_stack(sd, m, 4, impl=LL)
     assert L.e0_read_status(sd.status) == 0
+    worst, n_ex = check_stack(m, traces, (0, 1, 2, 3))
+    print("K", K, "prerouter", prerouter, "worst", worst, "tie-exempt", n_ex)
+    del sd
+    torch.cuda.empty_cache()
+
+
+def test_stack_range_launches_equal_one_launch(L, stack35):
+    """A token split into two launches at any layer gives the same bits as one."""
+    m, sd = stack35
+    from int4_gathered_expert_gb300 import lib
+    a = run_stack(sd, m, 3, impl=LL)
+    sd.prepare()
     for t in range(3):
-        assert rel_l2(b[t]["r"], a[t]["r"]) < 1e-4, t
-        same = (a[t]["inds"] == b[t]["inds"]).all(axis=1)
-        assert same.mean() > 0.95, (t, same.mean())
+        x = torch.from_numpy(m.x[t]).cuda()
+        split = (7, 22, 39)[t]
+        lib.e0_stack_step_range(x, None, sd.ws, 0, split, sd.trace, sd.status)
+        lib.e0_stack_step_range(None, sd.r_out, sd.ws, split, sd.L, sd.trace, sd.status)
+        b = snapshot(sd)
+        for k in ("r", "inds", "w", "head_logits", "pred_inds"):
+            assert np.array_equal(a[t][k], b[k]), (t, k)
+    assert L.e0_read_status(sd.status) == 0
+
+
+def _run_streamed(ss, sd, X, n_tok, overlap=True):
+    got = []
+    ss.start(X[0])
+    torch.cuda.synchronize()
+    got.append(snapshot(sd))
+    for t in range(1, n_tok):
+        ss.step(X[t], overlap=overlap)
+        torch.cuda.synchronize()
+        got.append(snapshot(sd))
+    return got
 
 
 def _tiny_stream_model():
@@ -179,33 +255,19 @@ def _tiny_stream_model():
 
 
 @pytest.mark.parametrize("overlap", [True, False])
-def test_streamed_stack_matches_resident(L, overlap):
+def test_streamed_stack_matches_oracle(L, overlap):
     """Host-tier staged streaming: the consumer layers hold 2K slots filled from
     pinned host memory with the experts the prerouter predicted one token
     earlier, copied on a second stream while the other half of the token runs.
-    Every token must agree with the resident-bank run (the deterministic
-    persistent kernel), with no slot miss."""
+    Every token is teacher-forced against the oracle, with no slot miss."""
     from int4_gathered_expert_gb300.model import StackDev, StreamedStack
     m = _tiny_stream_model()
-    ref = StackDev(m, trace=True)
-    want = run_stack(ref, m, 6, impl=0)
     sd = StackDev(m, trace=True)
     ss = StreamedStack(sd, split=5)
     assert ss.batch1 == [2, 3] and ss.batch2 == [5, 6, 7]
-    X = torch.from_numpy(m.x).cuda()
-    got = []
-    ss.start(X[0])
-    torch.cuda.synchronize()
-    got.append({k: v.cpu().numpy().copy() for k, v in sd.tr.items()})
-    for t in range(1, 6):
-        ss.step(X[t], overlap=overlap)
-        torch.cuda.synchronize()
-        got.append({k: v.cpu().numpy().copy() for k, v in sd.tr.items()})
+    got = _run_streamed(ss, sd, torch.from_numpy(m.x).cuda(), 6, overlap)
     assert L.e0_read_status(sd.status) == 0
-    for t in range(6):
-        assert rel_l2(got[t]["r"], want[t]["r"]) < 1e-4, t
-        same = (got[t]["inds"] == want[t]["inds"]).all(axis=1)
-        assert same.mean() > 0.9, (t, same.mean())
+    check_stack(m, got, range(6))
     # the staged layers really run from their slot pools: each holds at most 2K experts
     for l in ss.staged:
         tab = ss.pools[l].table.cpu().numpy()
@@ -215,35 +277,51 @@ def test_streamed_stack_matches_resident(L, overlap):
 @pytest.mark.parametrize("capacity", [3, 64])
 def test_streamed_stack_with_expert_cache(L, capacity):
     """Staged streaming with a cross-layer LRU cache of expert bundles in front
-    of the host bank: transparent (same tokens as the resident run), and the
-    counters add up (every copy is a hit or a miss; a cache smaller than the
-    working set evicts)."""
+    of the host bank: oracle results token by token, and the counters add up
+    (every copy is a hit or a miss; a cache smaller than the working set evicts)."""
     from int4_gathered_expert_gb300.model import ExpertCacheDev, StackDev, StreamedStack
     m = _tiny_stream_model()
-    ref = StackDev(m, trace=True)
-    want = run_stack(ref, m, 6, impl=0)
     sd = StackDev(m, trace=True)
     cache = ExpertCacheDev(capacity, sd.L, sd.H, sd.I, sd.E)
     ss = StreamedStack(sd, split=5, cache=cache)
     X = torch.from_numpy(m.x).cuda()
     copies = 0
-    occ = None
     ss.start(X[0])
-    got = [{k: v.cpu().numpy().copy() for k, v in sd.tr.items()}]
+    got = [snapshot(sd)]
     occ = {l: ss.pools[l].occupant.cpu().numpy().copy() for l in ss.staged}
     copies += sum(int((o >= 0).sum()) for o in occ.values())
     for t in range(1, 6):
         ss.step(X[t])
         torch.cuda.synchronize()
-        got.append({k: v.cpu().numpy().copy() for k, v in sd.tr.items()})
+        got.append(snapshot(sd))
         for l in ss.staged:
             now = ss.pools[l].occupant.cpu().numpy()
             copies += int((now != occ[l]).sum())
             occ[l] = now.copy()
     assert L.e0_read_status(sd.status) == 0
-    for t in range(6):
-        assert rel_l2(got[t]["r"], want[t]["r"]) < 1e-4, t
+    check_stack(m, got, range(6))
     st = cache.stats()
     assert st["hits"] + st["misses"] == copies
     if capacity < 5 * 4:
         assert st["evictions"] > 0
+
+
+@pytest.mark.parametrize("cache_capacity", [0, 64])
+def test_streamed_stack_35b_shape_matches_oracle(L, cache_capacity):
+    """Staged streaming (and with a 64-bundle LRU in front of the host bank) on
+    the 35B layer shape: 12 layers, heads owned by 2..10, two launches a token
+    split at layer 6, 2K = 8 slots per staged layer; teacher-forced against the
+    oracle on every token."""
+    from int4_gathered_expert_gb300.model import ExpertCacheDev, StackDev, StreamedStack
+    shape = dataclasses.replace(synth.STACK35B, n_layers=12, owners=tuple(range(2, 11)), seed=31)
+    m = synth.stack_model(shape, n_tokens=5)
+    sd = StackDev(m, trace=True)
+    cache = ExpertCacheDev(cache_capacity, sd.L, sd.H, sd.I, sd.E) if cache_capacity else None
+    ss = StreamedStack(sd, split=6, cache=cache)
+    assert ss.batch1 == [3, 4] and ss.batch2 == [6, 7, 8, 9, 10, 11]
+    got = _run_streamed(ss, sd, torch.from_numpy(m.x).cuda(), 5)
+    assert L.e0_read_status(sd.status) == 0
+    worst, n_ex = check_stack(m, got, range(5))
+    print("35B-shape streaming, cache", cache_capacity, "worst", worst, "tie-exempt", n_ex)
+    del ss, sd
+    torch.cuda.empty_cache()

@@ -53,4 +53,4 @@ def test_single_process_helpers():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.whole_job_rate(100, 1, 0.5) == 200.0
-    assert bench.LAUNCHES_PER_TOKEN[2] == 1
+    assert bench.LAUNCHES_PER_TOKEN[3] == 1
