@@ -971,14 +971,18 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
             }
 
             // ---- 4. gather the a-words (quantised by warp, one half-group unit
-            // each), the partial sums of z_d, and the hidden words of owner l-1's head
+            // each), the partial sums of z_d, and the hidden words of owner l-1's head.
+            // Only a CTA with down rows reads the a-words and z_d sums: one without
+            // rows publishes no residual word, so nothing keeps the other CTAs from
+            // running a layer ahead and overwriting these words while it still reads them.
+            const int nua = P.J1 > P.J0 ? P.NU : 0;
             unsigned long long aw[LL_MAXQ];
 #pragma unroll
             for (int m = 0; m < LL_MAXQ; ++m) {
                 const int u = warp + LL_NW * m;
-                if (u < P.NU) aw[m] = ll_get(S.llA + u * 32 + lane);
+                if (u < nua) aw[m] = ll_get(S.llA + u * 32 + lane);
             }
-            const int nzd = P.lora ? P.nsh * rank : 0;
+            const int nzd = P.lora && P.J1 > P.J0 ? P.nsh * rank : 0;
             unsigned long long zw = 0, hw = 0;
             const unsigned long long* zdw = S.llZd + (size_t)(tid / (rank > 0 ? rank : 1)) * LL_RANK +
                                             (rank > 0 ? tid % rank : 0);
@@ -988,7 +992,7 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
 #pragma unroll
             for (int m = 0; m < LL_MAXQ; ++m) {
                 const int u = warp + LL_NW * m;
-                if (u < P.NU) {
+                if (u < nua) {
                     const float v = ll_take(aw[m], S.llA + u * 32 + lane, ep, cx);
                     quantize_half_warp(v, apl + u * 4, axg + u, lane);
                 }
