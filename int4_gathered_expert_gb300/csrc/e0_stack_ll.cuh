@@ -719,8 +719,9 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
         };
 
         if (warp == PROD) {
-            // ---- prefetch of layer l + D into L2
-            if (l + pf_dist < le) {
+            // ---- prefetch of layer l + D into L2 (D = 0: none; the bulk copies
+            // already fetch layer l)
+            if (pf_dist > 0 && l + pf_dist < le) {
                 const int m = l + pf_dist;
                 const bool nat = layer_native(S, lyr[m], t);
                 ll_prefetch_layer<C>(lyr, Lz, slot_s, m, nat, !nat, false, c, nb, lane);
