@@ -5,17 +5,20 @@ One step = 256 consecutive decode tokens of an AR(1) token stream through the
 40 layers (H=2048, I=512, E=256, softmax-top-4, shared expert with an
 unmerged rank-16 LoRA, 33 prerouter heads owned by layers 6..38 whose
 predictions route layers 7..39 one token later).  Each token is one launch of
-the cluster whole-token kernel (--kernel-impl 2; 0 = persistent cooperative
-kernel, 1 = per-phase chain).  Weights are synthetic (seeded), resident in HBM
-(18.1 GB expert bank); every token streams ~484 MB of weights, far more than
-the 129 MB L2, so no flush is needed between iterations.
+the flag-carrying-word whole-token kernel (--kernel-impl 3; 0 = persistent
+cooperative kernel, 1 = per-phase chain).  Weights are synthetic (seeded),
+resident in HBM (18.1 GB expert bank); every token streams ~484 MB of
+weights, far more than the 129 MB L2, so no flush is needed between
+iterations.
 
 The same JSON line also carries: the end-to-end rate through the C ABI with
-host buffers (e2e), the CPU oracle (cpu_baseline), the host-tier staged
-streaming run (streaming: consumer layers' experts in pinned host memory,
-copied one token ahead of use), and the T=4096 whole-layer prefill of the
-35B and the 8B tier (prefill, prefill_8b).  --route-k and --no-prerouter give
-the K / prerouter variants.
+host buffers (e2e), the CPU oracle on all host cores (cpu_baseline) and on one
+thread for the single-layer workloads (cpu_oracle_one_thread), the K x
+prerouter on/off sweep on the same weights (route_sweep), the 35B-tier single
+layer alone at T=1 and T=8 (block_35b), the 8B-tier 24-layer stack
+(stack_8b), the host-tier staged streaming run (streaming: consumer layers'
+experts in pinned host memory, copied one token ahead of use), and the
+T=4096 whole-layer prefill of the 35B and the 8B tier (prefill, prefill_8b).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -62,6 +65,8 @@ def parse():
     p.add_argument("--no-prerouter", action="store_true",
                    help="every layer routes with its own router; no prerouter heads")
     p.add_argument("--no-streaming", action="store_true", help="skip the host-tier staged-streaming measurement")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the K / prerouter sweep, the single-layer block and the 8B-tier stack measurements")
     p.add_argument("--stream-split", type=int, default=22,
                    help="first layer of the second launch of a token in the staged-streaming run")
     return p.parse_args()
@@ -123,6 +128,227 @@ def run_prefill_bench(dev, reps: int = 5, tier: str = "35b"):
                          "peak_source": "MEASURED_PEAKS.json bf16_tflops (measured, fp16 = bf16 rate)"
                          if pk else "fallback"},
             "l2": "flushed (256 MB write) before each timed call", "device_status": int(st.item())}
+
+
+# ---------------------------------------------------------------- one layer alone
+
+
+def _timed(fn, stream, flush, reps: int):
+    """Median device time (s) of fn() on ``stream``, the L2 flushed (a 256 MB
+    write) before each call."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / 1e3)
+    return float(np.median(times))
+
+
+def run_block_bench(dev, reps: int = 20):
+    """The 35B-tier single decode layer (H=2048, I=512, E=256, K=4) at T=1 and
+    T=8: the MoE block with native routing on the resident bank, the same
+    block on a 2KT-slot staged pool with the routing handed in, the slot
+    update that fills that pool, and the prerouter head.  Bytes are the
+    weights the call must read: the union of the selected experts (plus the
+    router for native routing, the head's weights for the head)."""
+    import torch
+    from int4_gathered_expert_gb300 import lib as L
+    from int4_gathered_expert_gb300 import synth
+    from int4_gathered_expert_gb300.model import HeadDev, SlotPoolDev
+    d = synth.layer35b(1, T=8)
+    s = d["shape"]
+    eb = synth.expert_nbytes(s)
+    pool = SlotPoolDev.resident(d["bank"], s.H, s.I, dev)
+    Wr = torch.from_numpy(d["router"]).to(dev)
+    head = HeadDev(d["head"], s.H, s.E, dev)
+    head_bytes = sum(int(np.asarray(v).nbytes) for v in d["head"].values())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    pk = peaks()
+    peak = pk["hbm_gbs"] if pk else 6800.0
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {"workload": "35B-tier single layer decode: H=2048, I=512, E=256, softmax-top-k K=4, prerouter head "
+                       "hidden 512; seed 1", "l2": "flushed (256 MB write) before each timed call",
+           "peak_gbs": peak}
+    x = torch.from_numpy(d["x"]).to(dev)
+    for T in (1, 8):
+        h = torch.empty((T, s.H), dtype=torch.float32, device=dev)
+        L.e0_rmsnorm(x[:T].contiguous(), T, s.H, 1e-6, h)
+        ws_bytes = L.e0_workspace_size(0, T, s.H, s.I, s.E, s.K)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        y = torch.empty((T, s.H), dtype=torch.float32, device=dev)
+        io = torch.empty((T, s.K), dtype=torch.int32, device=dev)
+        wo = torch.empty((T, s.K), dtype=torch.float32, device=dev)
+        rp = L.route_params(K=s.K)
+
+        def native():
+            L.e0_moe_block_forward(h, T, pool.desc, Wr, rp, None, None, None, y, io, wo, ws, ws_bytes, st,
+                                   stream=stream)
+        t_nat = _timed(native, stream, flush, reps)
+        inds = io.cpu().numpy()
+        n_union = len(set(int(e) for e in inds.ravel()))
+        b_nat = n_union * eb + s.E * s.H * 2
+        # staged: 2KT slots filled from the resident bank (previous set, then this one)
+        n_slots = 2 * s.K * T
+        staged = SlotPoolDev(s.H, s.I, s.E, n_slots, dev)
+        prev = torch.from_numpy(d["inds_prev"][:T].ravel().astype(np.int32)).to(dev)
+        cur = io.reshape(-1).clone()
+        L.e0_slot_update(staged.desc, prev, prev.numel(), None, 0, pool.data, st, stream=stream)
+        torch.cuda.synchronize()
+        tab0, occ0 = staged.table.clone(), staged.occupant.clone()
+        n_new = len(set(cur.cpu().tolist()) - set(prev.cpu().tolist()))
+
+        def update():
+            staged.table.copy_(tab0)
+            staged.occupant.copy_(occ0)
+            L.e0_slot_update(staged.desc, cur, cur.numel(), prev, prev.numel(), pool.data, st, stream=stream)
+        t_upd = _timed(update, stream, flush, reps)
+        wi = wo.clone()
+
+        def staged_block():
+            L.e0_moe_block_forward(h, T, staged.desc, None, rp, cur, wi, None, y, io, wo, ws, ws_bytes, st,
+                                   stream=stream)
+        t_stg = _timed(staged_block, stream, flush, reps)
+        b_stg = n_union * eb
+        # prerouter head of the same layer
+        hws_bytes = L.e0_workspace_size(1, T, s.H, head.hidden, s.E, s.K)
+        hws = torch.empty(hws_bytes, dtype=torch.uint8, device=dev)
+        z = torch.empty((T, s.E), dtype=torch.float32, device=dev)
+        ni = torch.empty((T, s.K), dtype=torch.int32, device=dev)
+        nw = torch.empty((T, s.K), dtype=torch.float32, device=dev)
+        pv = prev.reshape(T, s.K)
+
+        def head_call():
+            L.e0_prerouter_forward(h, T, io, pv, head.desc, rp, z, ni, nw, hws, hws_bytes, st, stream=stream)
+        t_head = _timed(head_call, stream, flush, reps)
+        out["T%d" % T] = {
+            "block_native": {"us": t_nat * 1e6, "bytes": b_nat, "gbs": b_nat / t_nat / 1e9,
+                             "frac": b_nat / t_nat / 1e9 / peak, "experts_read": n_union},
+            "block_staged": {"us": t_stg * 1e6, "bytes": b_stg, "gbs": b_stg / t_stg / 1e9,
+                             "frac": b_stg / t_stg / 1e9 / peak, "n_slots": n_slots},
+            "slot_update": {"us": t_upd * 1e6, "experts_copied": n_new,
+                            "copy_gbs": n_new * eb * 2 / t_upd / 1e9 if n_new else None},
+            "prerouter": {"us": t_head * 1e6, "bytes": head_bytes, "gbs": head_bytes / t_head / 1e9}}
+    out["device_status"] = int(st.item())
+    return out
+
+
+# ---------------------------------------------------------------- other stacks and variants
+
+
+def _time_tokens(sd, X, t0: int, t1: int, stream, impl: int = 3) -> float:
+    """Seconds per token of sd over tokens t0..t1 (device time, one launch a token)."""
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for t in range(t0, t1):
+            sd.step(X[t], impl=impl, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / (t1 - t0)
+
+
+def run_stack8b_bench(dev, n_warm: int = 8, n_timed: int = 128):
+    """8B-tier 24-layer stack decode (H=1536, I=384, E=128, sigmoid-group n=8
+    G=4 s=2.5 K=8, heads owned by 7..22), one flag-carrying-word launch a
+    token; token 0 (every layer routes natively) is in the warm-up."""
+    import torch
+    from int4_gathered_expert_gb300 import synth
+    from int4_gathered_expert_gb300.model import StackDev
+    shape = synth.STACK8B
+    model = synth.stack_model(shape, n_tokens=n_warm + n_timed)
+    sd = StackDev(model, device=dev)
+    X = torch.from_numpy(model.x).to(dev)
+    stream = torch.cuda.Stream()
+    _time_tokens(sd, X, 0, n_warm, stream)
+    s_tok = _time_tokens(sd, X, n_warm, n_warm + n_timed, stream)
+    nb = bytes_per_token(shape, native_layers=sum(1 for l in range(shape.n_layers) if l not in shape.consumers))
+    pk = peaks()
+    peak = pk["hbm_gbs"] if pk else 6800.0
+    st = int(sd.status.item())
+    del sd
+    torch.cuda.empty_cache()
+    return {"workload": "8B-tier 24-layer stack decode, batch 1: H=1536, I=384, E=128, sigmoid group-limited "
+                        "n=8 G=4 s=2.5 K=8, 16 prerouter heads (owners 7..22, hidden 512), AR(1) rho=0.8 stream",
+            "value": 1.0 / s_tok, "unit": "tok/s", "us_per_token": s_tok * 1e6, "tokens": n_timed,
+            "bytes_per_token": nb, "weight_gbs": nb["total"] / s_tok / 1e9,
+            "roofline": {"bound": "hbm", "achieved": nb["total"] / s_tok / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": nb["total"] / s_tok / 1e9 / peak, "kernel": "k_stack_ll"},
+            "device_status": st}
+
+
+def run_route_sweep(sd, X, n_warm: int = 8, n_timed: int = 96):
+    """The 35B-tier stack with K = 2, 4, 8 routed experts, each with the
+    prerouter on (layers 7..39 take the prediction made one token earlier) and
+    off (every layer routes with its own router, no heads): same weights."""
+    import torch
+    stream = torch.cuda.Stream()
+    rows = []
+    for K in (2, 4, 8):
+        r = {"K": K}
+        for on in (True, False):
+            v = sd.variant(K=K, prerouter=on)
+            _time_tokens(v, X, 0, n_warm, stream)
+            s_tok = _time_tokens(v, X, n_warm, n_warm + n_timed, stream)
+            key = "on" if on else "off"
+            r[key] = {"tok_s": 1.0 / s_tok, "us_per_token": s_tok * 1e6, "device_status": int(v.status.item())}
+            del v
+        r["on_over_off"] = r["on"]["tok_s"] / r["off"]["tok_s"]
+        rows.append(r)
+    torch.cuda.empty_cache()
+    return {"workload": "35B-tier 40-layer stack, K in {2, 4, 8} x prerouter on/off, same weights and stream",
+            "tokens": n_timed, "rows": rows}
+
+
+ORACLE_ONE_THREAD = r"""
+import json, sys, time
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from oracle import e0_oracle as O
+from int4_gathered_expert_gb300 import synth
+res = {}
+def blk(d, T):
+    s = d["shape"]
+    hh = O.rmsnorm(d["x"][:T].astype(np.float64))
+    t0 = time.perf_counter()
+    rt = O.route_softmax_topk(O.router_logits(d["router"], hh), s.K)
+    O.moe_block(hh, O.BankExperts(d["bank"]), rt.inds, rt.w)
+    return time.perf_counter() - t0
+d = synth.tiny_layer(0, T=8)
+blk(d, 8)
+res["tiny_T8_ms"] = 1e3 * min(blk(d, 8) for _ in range(3))
+d = synth.layer35b(1, T=8)
+for T in (1, 8):
+    res["l35b_T%d_ms" % T] = 1e3 * blk(d, T)
+print(json.dumps(res))
+"""
+
+
+def time_oracle_one_thread():
+    """The oracle's MoE block (routing + experts) on one host thread: the tiny
+    layer (T=8) and the 35B-tier single layer (T=1, T=8)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        p = subprocess.run([sys.executable, "-c", ORACLE_ONE_THREAD, ROOT], env=env, capture_output=True, text=True,
+                           timeout=600)
+        r = json.loads(p.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as ex:
+        return {"error": repr(ex)[:200]}
+    r.update({"cores": 1, "kind": "oracle",
+              "sample": "one call of the float64 numpy oracle's routing + MoE block, BLAS limited to one thread"})
+    return r
 
 
 # ---------------------------------------------------------------- host-tier staged streaming
@@ -551,6 +777,11 @@ def run_gb300(args):
                "sample": f"first {n_cpu} tokens of the same stream (token 0 routes all 40 layers natively) "
                          "through the 40-layer stack, float64 numpy oracle"}
 
+    sweep = None
+    if rank == 0 and not args.no_extras and args.kernel_impl == 3 and args.layers == 40 and args.route_k == 4 \
+            and not args.no_prerouter:
+        sweep = run_route_sweep(sd, X)
+
     streaming = None
     if rank == 0 and not args.no_streaming and args.kernel_impl == 3:
         del sd
@@ -561,9 +792,22 @@ def run_gb300(args):
             streaming = {"error": repr(ex)[:300]}
         sd = None
 
+    block = stack8b = oracle1 = None
+    if rank == 0 and not args.no_extras:
+        del sd
+        sd = None
+        torch.cuda.empty_cache()
+        block = run_block_bench(dev)
+        torch.cuda.empty_cache()
+        stack8b = run_stack8b_bench(dev)
+        torch.cuda.empty_cache()
+        if ws == 1 and not args.no_cpu:
+            oracle1 = time_oracle_one_thread()
+
     prefill = prefill8 = None
     if rank == 0 and not args.no_prefill:
         del sd
+        sd = None
         torch.cuda.empty_cache()
         prefill = run_prefill_bench(dev)
         torch.cuda.empty_cache()
@@ -591,7 +835,10 @@ def run_gb300(args):
                              "frac": achieved / peak, "traffic": traffic,
                              "kernel": kname, "launch_us": mean_launch_s * 1e6,
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback"},
-                "cpu_baseline": cpu, "e2e": e2e, "prefill": prefill, "prefill_8b": prefill8, "streaming": streaming, "gpu_launches": n_timed * LAUNCHES_PER_TOKEN.get(args.kernel_impl, 6 * shape.n_layers + 1),
+                "cpu_baseline": cpu, "cpu_oracle_one_thread": oracle1, "e2e": e2e, "prefill": prefill,
+                "prefill_8b": prefill8, "stack_8b": stack8b, "block_35b": block, "route_sweep": sweep,
+                "streaming": streaming,
+                "gpu_launches": n_timed * LAUNCHES_PER_TOKEN.get(args.kernel_impl, 6 * shape.n_layers + 1),
                 "clocks": clocks, "device_status": st}
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -306,7 +306,11 @@ size_t e0_stack_workspace_size(int L, int H, int I, int E, int K, int head_hidde
  * layer's weight slices.  Environment (read here): E0MOE_WAIT_US (1..10^7,
  * default 200000) is the longest a device-side wait of impl 3 polls before
  * it gives up with E0_ST_TIMEOUT; E0MOE_PF_DIST (0..64, default 0) makes
- * impl 3 also prefetch the weights of that many layers ahead into L2. */
+ * impl 3 also prefetch the weights of that many layers ahead into L2;
+ * E0MOE_LL_FREE_SMS (0..64, default 0) launches impl 3 on that many fewer
+ * SMs, so that kernels on other streams (host-tier slot copies) can run
+ * beside it (a stack whose work split no longer fits then gets
+ * E0_ERR_UNSUPPORTED from impl 3). */
 int e0_stack_prepare(const e0_stack_layer* layers, int L, int H, int I, int E,
                      const e0_route_params* rp, void* ws, size_t ws_bytes, e0_stream_t stream);
 

@@ -118,11 +118,21 @@ __global__ void k_slot_copy(const int32_t* table, const int32_t* occupant, uint8
     __syncthreads();
     const size_t chunks = sbytes / 16;
     const size_t total = chunks * P.n;
-    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (size_t)gridDim.x * blockDim.x) {
-        const int c = (int)(q / chunks);
-        const size_t off = (q % chunks) * 16;
-        const uint4 v = *reinterpret_cast<const uint4*>(bank + (size_t)P.e[c] * sbytes + off);
-        *reinterpret_cast<uint4*>(pool + (size_t)P.s[c] * sbytes + off) = v;
+    // four 16-byte loads in flight per thread (the bank may be host memory)
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t q0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q0 < total; q0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            if (q < total)
+                v[u] = *reinterpret_cast<const uint4*>(bank + (size_t)P.e[q / chunks] * sbytes + (q % chunks) * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            if (q < total) *reinterpret_cast<uint4*>(pool + (size_t)P.s[q / chunks] * sbytes + (q % chunks) * 16) = v[u];
+        }
     }
 }
 
@@ -224,14 +234,31 @@ __global__ void k_cache_copy(uint8_t* pool, const uint8_t* bank, e0_expert_cache
     const int n = plan[0];
     const size_t chunks = sbytes / 16;
     const size_t total = chunks * (size_t)n;
-    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (size_t)gridDim.x * blockDim.x) {
-        const int i = (int)(q / chunks);
-        const size_t off = (q % chunks) * 16;
-        const int e = plan[4 + 4 * i], s = plan[4 + 4 * i + 1], src = plan[4 + 4 * i + 2], fill = plan[4 + 4 * i + 3];
-        const uint8_t* from = src >= 0 ? c.data + (size_t)src * sbytes : bank + (size_t)e * sbytes;
-        const uint4 v = *reinterpret_cast<const uint4*>(from + off);
-        *reinterpret_cast<uint4*>(pool + (size_t)s * sbytes + off) = v;
-        if (fill >= 0) *reinterpret_cast<uint4*>(c.data + (size_t)fill * sbytes + off) = v;
+    // four 16-byte loads in flight per thread (the bank may be host memory)
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t q0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q0 < total; q0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            if (q < total) {
+                const int i = (int)(q / chunks);
+                const int e = plan[4 + 4 * i], src = plan[4 + 4 * i + 2];
+                const uint8_t* from = src >= 0 ? c.data + (size_t)src * sbytes : bank + (size_t)e * sbytes;
+                v[u] = *reinterpret_cast<const uint4*>(from + (q % chunks) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            if (q < total) {
+                const int i = (int)(q / chunks);
+                const size_t off = (q % chunks) * 16;
+                const int s = plan[4 + 4 * i + 1], fill = plan[4 + 4 * i + 3];
+                *reinterpret_cast<uint4*>(pool + (size_t)s * sbytes + off) = v[u];
+                if (fill >= 0) *reinterpret_cast<uint4*>(c.data + (size_t)fill * sbytes + off) = v[u];
+            }
+        }
     }
 }
 
@@ -302,6 +329,7 @@ struct StackHdr {
     uint32_t ll_abort;         // set when a CTA gave up waiting
     unsigned long long ll_wait_ns;  // a poll gives up after this much device time
     int32_t grid3, smem3, pf_dist, ll_ok;
+    int32_t free_sms;  // SMs impl 3 leaves to other streams; the prefetch copies run on that many CTAs
 };
 
 struct TraceP {
@@ -774,9 +802,9 @@ int pack_experts(const e0_expert_q* src, int n, const e0_slot_pool* dst, const i
 }
 
 int slot_update(const e0_slot_pool* p, const int32_t* next, int n_next, const int32_t* cur, int n_cur,
-                const uint8_t* bank, uint32_t* st, cudaStream_t s) {
+                const uint8_t* bank, uint32_t* st, cudaStream_t s, int grid) {
     const size_t sb = slot_bytes(p->H, p->I);
-    k_slot_copy<<<num_sms(), 512, 0, s>>>(p->slot_table, p->occupant, p->data, p->n_slots, p->E, next, n_next, cur,
+    k_slot_copy<<<grid > 0 ? grid : num_sms(), 512, 0, s>>>(p->slot_table, p->occupant, p->data, p->n_slots, p->E, next, n_next, cur,
                                           n_cur, bank, sb);
     if (launch_ok() != E0_OK) return E0_ERR_CUDA;
     k_slot_commit<<<1, 32, 0, s>>>(p->slot_table, p->occupant, p->n_slots, p->E, next, n_next, cur, n_cur, st);
@@ -986,8 +1014,17 @@ static std::map<const void*, StackHdr> g_stacks;
 // layer's work split fits the kernel's per-CTA limits (ll_ok = 0: impl 3
 // returns E0_ERR_UNSUPPORTED for this stack).
 static void ll_geometry(StackHdr* hdr, const e0_stack_layer* layers, int L, int H, int I, int E, int K) {
-    const int nb = num_sms();
+    // SMs left free for kernels on other streams (the host-tier copies of a
+    // streamed stack): a cooperative launch cannot start until every one of its
+    // CTAs is resident, so a grid over all SMs waits out any running copy kernel
+    int free_sms = 0;
+    if (const char* env = getenv("E0MOE_LL_FREE_SMS")) {
+        const int v = atoi(env);
+        if (v >= 0 && v <= 64) free_sms = v;
+    }
+    const int nb = num_sms() - free_sms > 1 ? num_sms() - free_sms : 1;
     hdr->grid3 = nb;
+    hdr->free_sms = free_sms;
     hdr->pf_dist = LL_PF_DIST;
     if (const char* env = getenv("E0MOE_PF_DIST")) {
         const int v = atoi(env);
@@ -1178,7 +1215,7 @@ int stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* 
     if (!stack_hdr(ws, &hdr)) return E0_ERR_ARG;
     if (layer < 0 || layer >= hdr.L || t_next < 1) return E0_ERR_ARG;
     const int32_t* next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
-    return slot_update(pool, next, hdr.K, nullptr, 0, bank, st, s);
+    return slot_update(pool, next, hdr.K, nullptr, 0, bank, st, s, hdr.free_sms);
 }
 
 int stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot_pool* p, const uint8_t* bank,
@@ -1189,7 +1226,7 @@ int stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot
     if ((long)(layer + 1) * p->E > c->n_keys) return E0_ERR_ARG;
     const int32_t* next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
     k_cache_plan<<<1, 32, 0, s>>>(p->slot_table, p->occupant, p->n_slots, p->E, next, hdr.K, layer, *c);
-    k_cache_copy<<<num_sms(), 512, 0, s>>>(p->data, bank, *c, slot_bytes(p->H, p->I));
+    k_cache_copy<<<hdr.free_sms > 0 ? hdr.free_sms : num_sms(), 512, 0, s>>>(p->data, bank, *c, slot_bytes(p->H, p->I));
     k_slot_commit<<<1, 32, 0, s>>>(p->slot_table, p->occupant, p->n_slots, p->E, next, hdr.K, nullptr, 0, st);
     return launch_ok();
 }

@@ -15,7 +15,7 @@ size_t slot_bytes(int H, int I);
 int pack_experts(const e0_expert_q* src, int n, const e0_slot_pool* dst, const int32_t* dst_slots,
                  const int32_t* expert_ids, cudaStream_t s);
 int slot_update(const e0_slot_pool* p, const int32_t* next, int n_next, const int32_t* cur, int n_cur,
-                const uint8_t* bank, uint32_t* st, cudaStream_t s);
+                const uint8_t* bank, uint32_t* st, cudaStream_t s, int grid = 0);
 int stack_step_range(const float* x, float* r_out, void* ws, int lb, int le, const e0_stack_trace* trace, uint32_t* st,
                      cudaStream_t s);
 int stack_update_layers(void* ws, const e0_stack_layer* layers, int L, cudaStream_t s);

@@ -132,6 +132,30 @@ class StackDev:
                                                                            "pred_inds")])
         self.prepare()
 
+    def variant(self, K: Optional[int] = None, prerouter: bool = True, device="cuda") -> "StackDev":
+        """The same device weights with another routed-expert count K and/or
+        without the prerouter heads (every layer then routes with its own
+        router); its own workspace and status word, no trace."""
+        import copy
+        v = copy.copy(self)
+        s = self.shape.layer
+        v.K = self.K if K is None else int(K)
+        consumers = set(self.shape.consumers) if prerouter else set()
+        heads = self._hd_descs if prerouter else {}
+        v.layers = [L.StackLayer(self.pools[l].desc, self.routers[l].data_ptr(),
+                                 self._sh_descs[l] if self._sh_descs[l] is not None else None,
+                                 heads.get(l), 1 if (l in consumers and (l - 1) in heads) else 0)
+                    for l in range(self.L)]
+        v.rp = L.route_params(0 if s.route == "softmax_topk" else 1, v.K, s.n_groups, s.topk_groups, s.route_scale)
+        hidden = max([h.hidden for h in self.heads.values()], default=0) if prerouter else 0
+        v.ws_bytes = L.e0_stack_workspace_size(self.L, s.H, s.I, s.E, v.K, hidden)
+        v.ws = torch.empty(v.ws_bytes, dtype=torch.uint8, device=device)
+        v.status = torch.zeros(1, dtype=torch.int32, device=device)
+        v.r_out = torch.empty(s.H, dtype=torch.float32, device=device)
+        v.trace = None
+        v.prepare()
+        return v
+
     def prepare(self, stream=None):
         L.e0_stack_prepare(self.layers, self.H, self.I, self.E, self.rp, self.ws, self.ws_bytes, stream=stream)
 
@@ -164,7 +188,7 @@ class ExpertCacheDev:
 
 
 class StreamedStack:
-    """Host-tier staged streaming on top of a StackDev (cluster kernel).
+    """Host-tier staged streaming on top of a StackDev (flag-carrying-word kernel).
 
     Each staged layer keeps its experts (kernel layout) in pinned host memory
     and only 2K slots in device memory.  A token runs as two launches, layers
@@ -175,10 +199,24 @@ class StreamedStack:
     split - 1, whose prediction is final only once the token has ended but
     which the next token's first half uses, stays in the resident bank, as do
     the layers that route natively.  With an ExpertCacheDev the copies first
-    look in a cross-layer cache of recently used bundles in device memory."""
+    look in a cross-layer cache of recently used bundles in device memory.
+
+    The decode launches leave ``free_sms`` SMs to the copy kernels, which run
+    on that many blocks: a cooperative launch over every SM would wait for a
+    running copy kernel instead of overlapping it."""
 
     def __init__(self, sd: "StackDev", split: int, device="cuda", cache: Optional["ExpertCacheDev"] = None,
-                 host: Optional[dict] = None):
+                 host: Optional[dict] = None, free_sms: int = 24):
+        import os
+        old = os.environ.get("E0MOE_LL_FREE_SMS")
+        os.environ["E0MOE_LL_FREE_SMS"] = str(int(free_sms))
+        try:
+            sd.prepare()
+        finally:
+            if old is None:
+                del os.environ["E0MOE_LL_FREE_SMS"]
+            else:
+                os.environ["E0MOE_LL_FREE_SMS"] = old
         self.sd = sd
         self.split = split
         self.cache = cache

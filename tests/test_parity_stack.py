@@ -220,6 +220,29 @@ def test_35b_shape_route_k_and_prerouter_variants(L, K, prerouter):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("K,prerouter", [(2, True), (4, False)])
+def test_stack_variant_equals_fresh_stack(L, K, prerouter):
+    """StackDev.variant (the same device weights with another K, or without
+    heads) gives the bits of a stack built from scratch with that shape."""
+    from int4_gathered_expert_gb300.model import StackDev
+    base = dataclasses.replace(synth.STACK35B, n_layers=6, owners=tuple(range(1, 5)), seed=50)
+    m = synth.stack_model(base, n_tokens=4)
+    sd = StackDev(m)
+    v = sd.variant(K=K, prerouter=prerouter)
+    shape = dataclasses.replace(base, layer=dataclasses.replace(synth.L35B, K=K),
+                                owners=base.owners if prerouter else ())
+    m2 = synth.stack_model(shape, n_tokens=4)
+    fresh = StackDev(m2)
+    X = torch.from_numpy(m.x).cuda()
+    for t in range(4):
+        a = v.step(X[t], impl=LL).cpu().numpy()
+        b = fresh.step(X[t], impl=LL).cpu().numpy()
+        assert np.array_equal(a, b), t
+    assert L.e0_read_status(v.status) == 0 and L.e0_read_status(fresh.status) == 0
+    del sd, v, fresh
+    torch.cuda.empty_cache()
+
+
 def test_stack_range_launches_equal_one_launch(L, stack35):
     """A token split into two launches at any layer gives the same bits as one."""
     m, sd = stack35
