@@ -187,8 +187,9 @@ int e0_pack_experts(const e0_expert_q* src, int n, const e0_slot_pool* dst,
  * the next set.  Only changed slots are written; a resident bank (every
  * expert already has a slot) moves zero bytes.  No free slot left: sets
  * E0_ST_POOL_FULL and leaves that expert absent.  Ids outside [0, E) set
- * E0_ST_BAD_EXPERT and are skipped.  Single-block kernel; bytes move with
- * 16-byte copies by all of its threads. */
+ * E0_ST_BAD_EXPERT and are skipped.  One block plans the copies (each block
+ * replays the plan); the bytes move with 16-byte copies spread over one
+ * block per SM, then one block commits the tables. */
 int e0_slot_update(const e0_slot_pool* pool, const int32_t* d_inds_next, int n_next,
                    const int32_t* d_inds_cur, int n_cur, const uint8_t* bank,
                    uint32_t* d_status, e0_stream_t stream);

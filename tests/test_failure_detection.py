@@ -96,3 +96,40 @@ def test_stack_status_clean_on_a_normal_token(L):
     torch.cuda.synchronize()
     assert int(sd.status.item()) == 0
     assert L.e0_read_status(st) & L.E0_ST_TIMEOUT
+
+
+@pytest.mark.gpu
+def test_stack_ll_wait_limit_ends_in_timeout_and_recovers(L):
+    """impl 3 with a 1 us wait limit (E0MOE_WAIT_US, read at prepare): the
+    flag-carrying-word polls give up, the launch returns with E0_ST_TIMEOUT in
+    the status word (every block leaves after draining its own bulk copies),
+    and after a prepare with the normal limit the same stack decodes the same
+    bits as a stack that never timed out."""
+    _gpu()
+    from int4_gathered_expert_gb300 import synth
+    from int4_gathered_expert_gb300.model import StackDev
+    shape = synth.StackShape(layer=synth.TINY, n_layers=3, owners=(0, 1), shared_expert=True, seed=9)
+    m = synth.stack_model(shape, n_tokens=2, threads=2)
+    X = torch.from_numpy(m.x).cuda()
+    ref = StackDev(m, trace=False)
+    want = [ref.step(X[t], impl=3).cpu().numpy().copy() for t in range(2)]
+    assert int(ref.status.item()) == 0
+    sd = StackDev(m, trace=False)
+    old = os.environ.get("E0MOE_WAIT_US")
+    os.environ["E0MOE_WAIT_US"] = "1"
+    try:
+        sd.prepare()
+    finally:
+        if old is None:
+            del os.environ["E0MOE_WAIT_US"]
+        else:
+            os.environ["E0MOE_WAIT_US"] = old
+    sd.step(X[0], impl=3)
+    torch.cuda.synchronize()
+    assert L.e0_read_status(sd.status) & L.E0_ST_TIMEOUT
+    sd.status.zero_()
+    sd.prepare()
+    got = [sd.step(X[t], impl=3).cpu().numpy().copy() for t in range(2)]
+    assert int(sd.status.item()) == 0
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
