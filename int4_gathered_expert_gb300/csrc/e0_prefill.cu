@@ -331,24 +331,33 @@ static size_t router_gemm_smem() { return (size_t)STAGES * (BM * BK * 2 + BN * B
 // ------------------------------------------------------------------ persistent grouped GEMM with TMA-fed dequant
 
 // One CTA per SM loops over work items (tile of up to P2_BN tokens of one
-// expert x one 128-row slice of its weights).  Roles:
-//   warps 0-3  dequantise: thread r turns row r of the raw int4 tile (loaded
-//              by TMA into shared memory) into fp16 in the 128B-swizzled
-//              K-major operand layout;
+// expert x one 128-row slice of its weights).  Per K step the weight tile
+// goes HBM -> shared memory (raw int4 codes, 4 KB) -> registers -> tensor
+// memory (fp16, the MMA's A operand), so the dequantised tile costs no
+// shared-memory bandwidth; the token tile (B operand) is a TMA load into
+// shared memory.  Rings: raw code tiles P2_RAW_STAGES deep, operand stages
+// (A columns in tensor memory, B tile in shared memory) P2_OP_STAGES deep.
+// Roles:
+//   warps 0-3, 11-14  dequantise (two groups taking alternate K steps): thread
+//              r turns row r of a raw tile into fp16 and stores it into
+//              tensor-memory lane r of an operand stage;
 //   warps 4-7  epilogue: drain one of two TMEM accumulators while the MMA
 //              fills the other;
-//   warp 8     TMA: raw code tile (3-D map over the slot pool) + token tile;
-//   warp 9     TMEM allocation and the tcgen05.mma issue.
+//   warp 8     TMA: raw code tiles (tensor map over the slot pool), running
+//              up to P2_RAW_STAGES K steps ahead;
+//   warp 9     TMEM allocation and the tcgen05.mma issue;
+//   warp 10    TMA: token tiles into the operand stages.
 // In the gate/up GEMM a 128-row slice is 64 intermediate rows with the gate
 // and up rows interleaved (the slot layout stores them that way), so each
 // SwiGLU pair sits in adjacent TMEM lanes.
-constexpr int P2_STAGES = 5;
-constexpr int P2_THREADS = 320;
+constexpr int P2_OP_STAGES = 6;
+constexpr int P2_RAW_STAGES = 16;
+constexpr int P2_THREADS = 480;
 constexpr int P2_BN = 128;
-constexpr uint32_t P2_A = 128 * 128;       // fp16 operand tile
 constexpr uint32_t P2_B = P2_BN * 128;     // token tile
 constexpr uint32_t P2_RAW = 128 * 32;      // raw int4 codes of one K step
-constexpr uint32_t P2_STAGE = P2_A + P2_B + P2_RAW;
+constexpr uint32_t P2_OP = P2_B;           // shared memory of an operand stage
+constexpr uint32_t P2_ACOL = 2 * P2_BN;    // first tensor-memory column of the A tiles (after two accumulators)
 
 struct P2Item {
     int slot, row0, ncount, m;
@@ -392,7 +401,10 @@ E0_DEV void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst, int x,
 template <int MODE>
 __global__ void __launch_bounds__(P2_THREADS, 1)
     k_umma2(const __grid_constant__ CUtensorMap tmCodes, const __grid_constant__ CUtensorMap tmB, GemmP p) {
-    constexpr uint32_t TMEM_COLS = 2 * P2_BN;
+    // two fp32 accumulators of P2_BN columns, then one 32-column fp16 A tile
+    // (128 rows x 64 k) per operand stage
+    constexpr uint32_t TMEM_COLS = 512;
+    static_assert(P2_ACOL + 32 * P2_OP_STAGES <= TMEM_COLS, "tensor-memory columns");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int MT = MODE == MODE_GATEUP ? (2 * p.I) / 128 : p.H / 128;
     const int n_items = *p.n_tiles * MT;
@@ -400,19 +412,26 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + P2_STAGES * P2_STAGE);
-    uint64_t* a_full = raw_full + P2_STAGES;
-    uint64_t* empty = a_full + P2_STAGES;
-    uint64_t* acc_full = empty + P2_STAGES;
+    uint8_t* raw_ring = smem + P2_OP_STAGES * P2_OP;
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(raw_ring + P2_RAW_STAGES * P2_RAW);
+    uint64_t* raw_empty = raw_full + P2_RAW_STAGES;
+    uint64_t* a_full = raw_empty + P2_RAW_STAGES;
+    uint64_t* b_full = a_full + P2_OP_STAGES;
+    uint64_t* op_empty = b_full + P2_OP_STAGES;
+    uint64_t* acc_full = op_empty + P2_OP_STAGES;
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile uint32_t* abort = tmem_slot + 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < P2_STAGES; ++s) {
+        for (int s = 0; s < P2_RAW_STAGES; ++s) {
             mbar_init(&raw_full[s], 1);
-            mbar_init(&a_full[s], 128);
-            mbar_init(&empty[s], 1);
+            mbar_init(&raw_empty[s], 4);  // one arrival per dequantising warp
+        }
+        for (int s = 0; s < P2_OP_STAGES; ++s) {
+            mbar_init(&a_full[s], 4);
+            mbar_init(&b_full[s], 1);
+            mbar_init(&op_empty[s], 1);
         }
         for (int b2 = 0; b2 < 2; ++b2) {
             mbar_init(&acc_full[b2], 1);
@@ -427,11 +446,19 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const SlotLayout sl{p.H, p.I};
+    // a producer that stops early waits (bounded, abort flag ignored) for the
+    // copies it issued before the block can leave
+    const volatile uint32_t never = 0;
 
-    if (warp < 4) {
-        // ---------------- dequantisers
-        const int r = threadIdx.x;
-        uint32_t g = 0;
+    if (warp < 4 || warp >= 11) {
+        // ---------------- dequantisers: two groups of four warps take alternate
+        // K steps (warps 0-3 the even global steps, 11-14 the odd ones), so that
+        // one step's load -> convert -> tensor-memory store chain overlaps the
+        // other's; thread r handles weight row r, tensor-memory lane r
+        const int grp = warp < 4 ? 0 : 1;
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        uint32_t gbase = 0;  // global step of the item's first K step
         bool ok = true;
         for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
             const P2Item it = p2_item(p, idx, MT);
@@ -442,46 +469,64 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 if (MODE == MODE_GATEUP) sbp = ex + sl.gu_sb() + (size_t)wr * (p.H / GROUP) * 4;
                 else sbp = ex + sl.down_sb_off(wr, 0);  // group kk at + kk * DROWS * 4
             }
-            // (scale, bias) words of 8 K steps are loaded one chunk ahead of use
             const size_t sstep = MODE == MODE_GATEUP ? (size_t)4 : (size_t)DROWS * 4;
+            // this group's steps of the item: kk = kk0, kk0 + 2, ...
+            const int kk0 = (int)((gbase + (uint32_t)grp) & 1u);
+            const int n_own = nk > kk0 ? (nk - kk0 + 1) / 2 : 0;
+            // (scale, bias) words of 8 own steps are loaded one chunk ahead of use
             uint32_t sbw[8], sbn[8];
 #pragma unroll
-            for (int d = 0; d < 8; ++d) sbn[d] = (ex && d < nk) ? ldg_u32(sbp + (size_t)d * sstep) : 0u;
-            for (int k0 = 0; k0 < nk && ok; k0 += 8) {
+            for (int d = 0; d < 8; ++d) sbn[d] = (ex && d < n_own) ? ldg_u32(sbp + (size_t)(kk0 + 2 * d) * sstep) : 0u;
+            for (int i0 = 0; i0 < n_own && ok; i0 += 8) {
 #pragma unroll
                 for (int d = 0; d < 8; ++d) {
                     sbw[d] = sbn[d];
-                    sbn[d] = (ex && k0 + 8 + d < nk) ? ldg_u32(sbp + (size_t)(k0 + 8 + d) * sstep) : 0u;
+                    const int in = i0 + 8 + d;
+                    sbn[d] = (ex && in < n_own) ? ldg_u32(sbp + (size_t)(kk0 + 2 * in) * sstep) : 0u;
                 }
 #pragma unroll
                 for (int d = 0; d < 8; ++d) {
-                    const int kk = k0 + d;
-                    if (kk >= nk) break;
-                    const uint32_t s = g % P2_STAGES;
-                    if (!mbar_wait(&raw_full[s], (g / P2_STAGES) & 1, abort, WAIT_LIMIT_NS)) {
+                    const int i = i0 + d;
+                    if (i >= n_own) break;
+                    const uint32_t g = gbase + (uint32_t)(kk0 + 2 * i);
+                    const uint32_t rs = g % P2_RAW_STAGES, os = g % P2_OP_STAGES;
+                    const bool w = mbar_wait(&raw_full[rs], (g / P2_RAW_STAGES) & 1, abort, WAIT_LIMIT_NS) &&
+                                   mbar_wait(&op_empty[os], ((g / P2_OP_STAGES) + 1) & 1, abort, WAIT_LIMIT_NS);
+                    if (!__all_sync(0xffffffffu, w)) {  // the warp leaves together
                         ok = false;
                         *abort = 1;
                         atomicOr(p.err, 16u);
                         break;
                     }
-                    uint8_t* st = smem + s * P2_STAGE;
+                    tc_fence_after();
+                    uint32_t o[32];
                     if (ex) {
                         // gate/up raw tile: [128 rows][32 B]; down raw tile: [8 row
                         // blocks][2 half-groups][16 rows][16 B]
-                        const uint8_t* raw = st + P2_A + P2_B;
+                        const uint8_t* raw = raw_ring + rs * P2_RAW;
                         const uint8_t* rd = raw + ((r / DROWS) * 2 * DROWS + r % DROWS) * 16;
                         const uint4 c0 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 : rd);
                         const uint4 c1 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 + 16
                                                                                               : rd + DROWS * 16);
-                        dequant64_to_tile(c0, c1, sbw[d], st, r);
+                        dequant64_to_regs(c0, c1, sbw[d], o);
                     } else {
-                        zero_row_of_tile(st, r);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] = 0u;
                     }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&a_full[s]);
-                    ++g;
+                    tmem_st32(tmem + ((uint32_t)(q4 * 32) << 16) + P2_ACOL + os * 32, o);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    // once every lane is here, the warp has also used the values it
+                    // read from the raw slot (an arrive does not order those
+                    // generic-proxy reads before the next TMA write into the slot)
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&raw_empty[rs]);
+                        mbar_arrive(&a_full[os]);
+                    }
                 }
             }
+            gbase += (uint32_t)nk;
         }
     } else if (warp < 8) {
         // ---------------- epilogue
@@ -523,31 +568,60 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[buf]);
+            if (!have) break;
         }
     } else if (warp == 8) {
-        // ---------------- TMA producer
+        // ---------------- TMA: raw code tiles, up to P2_RAW_STAGES steps ahead
         if (lane == 0) {
             tma_prefetch_desc(&tmCodes);
-            tma_prefetch_desc(&tmB);
             uint32_t g = 0;
             bool ok = true;
             for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
                 const P2Item it = p2_item(p, idx, MT);
                 const int z = it.slot >= 0 ? it.slot : 0;
                 for (int kk = 0; kk < nk; ++kk, ++g) {
-                    const uint32_t s = g % P2_STAGES;
-                    if (!mbar_wait(&empty[s], ((g / P2_STAGES) + 1) & 1, abort, WAIT_LIMIT_NS)) {
+                    const uint32_t rs = g % P2_RAW_STAGES;
+                    if (!mbar_wait(&raw_empty[rs], ((g / P2_RAW_STAGES) + 1) & 1, abort, WAIT_LIMIT_NS)) {
                         ok = false;
                         *abort = 1;
                         atomicOr(p.err, 64u);
                         break;
                     }
-                    uint8_t* st = smem + s * P2_STAGE;
-                    mbar_arrive_expect_tx(&raw_full[s], P2_RAW + P2_B);
-                    if (MODE == MODE_GATEUP) tma_load_3d(&tmCodes, &raw_full[s], st + P2_A + P2_B, kk * 32, it.m * 128, z);
-                    else tma_load_5d(&tmCodes, &raw_full[s], st + P2_A + P2_B, 0, 0, 2 * kk, it.m * (128 / DROWS), z);
-                    tma_load_2d(&tmB, &raw_full[s], st + P2_A, kk * BK, it.row0);
+                    uint8_t* dst = raw_ring + rs * P2_RAW;
+                    mbar_arrive_expect_tx(&raw_full[rs], P2_RAW);
+                    if (MODE == MODE_GATEUP) tma_load_3d(&tmCodes, &raw_full[rs], dst, kk * 32, it.m * 128, z);
+                    else tma_load_5d(&tmCodes, &raw_full[rs], dst, 0, 0, 2 * kk, it.m * (128 / DROWS), z);
                 }
+            }
+            // the copies issued into each slot have landed before the block leaves
+            for (uint32_t d = 0; d < P2_RAW_STAGES && d < g; ++d) {
+                const uint32_t gl = g - 1 - d;
+                mbar_wait(&raw_full[gl % P2_RAW_STAGES], (gl / P2_RAW_STAGES) & 1, &never, WAIT_LIMIT_NS);
+            }
+        }
+    } else if (warp == 10) {
+        // ---------------- TMA: token tiles into the operand stages
+        if (lane == 0) {
+            tma_prefetch_desc(&tmB);
+            uint32_t g = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+                const P2Item it = p2_item(p, idx, MT);
+                for (int kk = 0; kk < nk; ++kk, ++g) {
+                    const uint32_t os = g % P2_OP_STAGES;
+                    if (!mbar_wait(&op_empty[os], ((g / P2_OP_STAGES) + 1) & 1, abort, WAIT_LIMIT_NS)) {
+                        ok = false;
+                        *abort = 1;
+                        atomicOr(p.err, 512u);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&b_full[os], P2_B);
+                    tma_load_2d(&tmB, &b_full[os], smem + os * P2_OP, kk * BK, it.row0);
+                }
+            }
+            for (uint32_t d = 0; d < P2_OP_STAGES && d < g; ++d) {
+                const uint32_t gl = g - 1 - d;
+                mbar_wait(&b_full[gl % P2_OP_STAGES], (gl / P2_OP_STAGES) & 1, &never, WAIT_LIMIT_NS);
             }
         }
     } else {
@@ -567,26 +641,31 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 const int n_mma = (it.ncount + 15) & ~15;
                 const uint32_t idesc = idesc_f16_f32(128, n_mma);
                 for (int kk = 0; kk < nk; ++kk, ++g) {
-                    const uint32_t s = g % P2_STAGES;
-                    const uint32_t ph = (g / P2_STAGES) & 1;
-                    if (!mbar_wait(&raw_full[s], ph, abort, WAIT_LIMIT_NS) ||
-                        !mbar_wait(&a_full[s], ph, abort, WAIT_LIMIT_NS)) {
+                    const uint32_t os = g % P2_OP_STAGES;
+                    const uint32_t ph = (g / P2_OP_STAGES) & 1;
+                    if (!mbar_wait(&b_full[os], ph, abort, WAIT_LIMIT_NS) ||
+                        !mbar_wait(&a_full[os], ph, abort, WAIT_LIMIT_NS)) {
                         ok = false;
                         *abort = 1;
                         atomicOr(p.err, 256u);
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + s * P2_STAGE);
-                    const uint32_t b_addr = a_addr + P2_A;
+                    const uint32_t b_addr = smem_u32(smem + os * P2_OP);
+                    const uint32_t a_tm = tmem + P2_ACOL + os * 32;
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)
-                        umma_f16(tmem + buf * P2_BN, sdesc_k_sw128(a_addr + j * 32), sdesc_k_sw128(b_addr + j * 32),
-                                 idesc, (kk | j) != 0);
-                    umma_commit(&empty[s]);
+                        umma_f16_ta(tmem + buf * P2_BN, a_tm + j * 8, sdesc_k_sw128(b_addr + j * 32), idesc,
+                                    (kk | j) != 0);
+                    umma_commit(&op_empty[os]);
                 }
                 if (!ok) break;
                 umma_commit(&acc_full[buf]);
+            }
+            // the MMAs issued have completed before TMEM is freed
+            if (g > 0) {
+                const uint32_t gl = g - 1;
+                mbar_wait(&op_empty[gl % P2_OP_STAGES], (gl / P2_OP_STAGES) & 1, &never, WAIT_LIMIT_NS);
             }
         }
     }
@@ -598,7 +677,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
     }
 }
 
-static size_t gemm2_smem() { return (size_t)P2_STAGES * P2_STAGE + 1024 + 256; }
+static size_t gemm2_smem() {
+    return (size_t)P2_OP_STAGES * P2_OP + (size_t)P2_RAW_STAGES * P2_RAW +
+           (2 * P2_RAW_STAGES + 3 * P2_OP_STAGES + 4) * 8 + 8 + 1024;
+}
 
 // ------------------------------------------------------------------ small prefill kernels
 
@@ -649,8 +731,108 @@ __device__ float topk_gap(const float* lg, int E, const float* bias, int K, int 
     return topk_gap_t<32>(lg, E, bias, K, lane);
 }
 
+// Sigmoid group-limited routing: a decision can change under a small logit
+// error only where the G-th and (G+1)-th group scores (sum of a group's two
+// largest sigmoids) are close, or where the K-th and (K+1)-th logits among
+// the experts of the kept groups are (the sigmoid is monotone).  A group
+// score moves by at most half the logit error (sigmoid' <= 1/4, two terms),
+// so one threshold serves both gaps.  One warp per token.
+template <int MAXM>
+__device__ bool sg_near_tie_t(const float* lg, int E, int n, int G, int K, float gap, int lane) {
+    const int per = E / n;
+    uint32_t key[MAXM];
+    float sg[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        const int e = lane + 32 * m;
+        key[m] = 0;
+        sg[m] = -INFINITY;
+        if (e < E) {
+            float x = __ldcg(lg + e);
+            if (!isfinite(x)) x = -INFINITY;
+            key[m] = float_order_key(x);
+            sg[m] = 1.f / (1.f + __expf(-x));
+        }
+    }
+    // group scores: lane g (< n) keeps the score of group g
+    float my_gs = -INFINITY;
+    for (int g = 0; g < n; ++g) {
+        float a = -INFINITY, b = -INFINITY;  // this lane's two largest sigmoids of group g
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) {
+            const int e = lane + 32 * m;
+            if (e < E && e / per == g) {
+                if (sg[m] > a) {
+                    b = a;
+                    a = sg[m];
+                } else if (sg[m] > b) {
+                    b = sg[m];
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float a2 = __shfl_xor_sync(0xffffffffu, a, o), b2 = __shfl_xor_sync(0xffffffffu, b, o);
+            const float hi = fmaxf(a, a2), lo = fmaxf(fminf(a, a2), fmaxf(b, b2));
+            a = hi;
+            b = lo;
+        }
+        if (lane == g) my_gs = a + b;
+    }
+    // G-th vs (G+1)-th group score; the kept groups (ties to the lower index)
+    uint32_t gkey = lane < n ? float_order_key(my_gs) : 0u;
+    uint32_t kept = 0;
+    float prev = 0.f, ggap = INFINITY;
+    for (int k = 0; k <= G && k < n; ++k) {
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, gkey);
+        const uint32_t wi = __reduce_min_sync(0xffffffffu, (gkey == mk && lane < n) ? (uint32_t)lane : 0xffffffffu);
+        if (wi >= 32u) break;
+        const float v = float_of_order_key(mk);
+        if (k == G) ggap = prev - v;  // only the boundary between kept and dropped groups matters
+        prev = v;
+        if (k < G) kept |= 1u << wi;
+        if ((uint32_t)lane == wi) gkey = 0;
+    }
+    if (G < n && ggap < gap) return true;
+    // K-th vs (K+1)-th logit among the kept groups' experts
+    uint32_t alive = 0;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        const int e = lane + 32 * m;
+        if (e < E && ((kept >> (e / per)) & 1u)) alive |= 1u << m;
+    }
+    float eprev = 0.f, egap = INFINITY;
+    for (int k = 0; k <= K; ++k) {
+        uint32_t bk = 0, bi = 0xffffffffu;
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m)
+            if (((alive >> m) & 1u) && key[m] > bk) {
+                bk = key[m];
+                bi = (uint32_t)(lane + 32 * m);
+            }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        if (mk == 0) break;
+        const uint32_t wi = __reduce_min_sync(0xffffffffu, bk == mk ? bi : 0xffffffffu);
+        if ((int)(wi & 31) == lane) alive &= ~(1u << (wi >> 5));
+        const float v = float_of_order_key(mk);
+        if (k > 0) egap = fminf(egap, eprev - v);
+        eprev = v;
+    }
+    return egap < gap;
+}
+
+__device__ bool sg_near_tie(const float* lg, int E, const RouteP& rp, float gap, int lane) {
+    if (rp.n_groups < 1 || rp.n_groups > 32 || E % rp.n_groups) return true;  // not expected: refine
+    if (E <= 32) return sg_near_tie_t<1>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
+    if (E <= 64) return sg_near_tie_t<2>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
+    if (E <= 128) return sg_near_tie_t<4>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
+    if (E <= 256) return sg_near_tie_t<8>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
+    if (E <= 512) return sg_near_tie_t<16>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
+    return sg_near_tie_t<32>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
+}
+
 // Route one token per warp from the tensor-core logits; flag tokens whose
-// top-(K+1) logits (plus bias) have a gap below REFINE_GAP.
+// routing a logit error below REFINE_GAP could change.
 __global__ void k_prefill_route(const float* logits, int T, int E, RouteP rp, int32_t* inds, float* w,
                                 int32_t* flag, uint32_t* st) {
     extern __shared__ float scr[];
@@ -659,10 +841,10 @@ __global__ void k_prefill_route(const float* logits, int T, int E, RouteP rp, in
     if (t >= T) return;
     const float* lg = logits + (size_t)t * E;
     route_warp(lg, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr + warp * E, st, lane);
-    // softmax routing is refined where two of the K+1 largest scores are close;
-    // sigmoid-group routing always is
-    const bool refine =
-        rp.mode != E0_ROUTE_SOFTMAX_TOPK || topk_gap(lg, E, rp.logit_bias, rp.K, lane) < REFINE_GAP;
+    // softmax routing is refined where two of the K+1 largest scores are close,
+    // sigmoid-group routing where a group or an expert decision is
+    const bool refine = rp.mode == E0_ROUTE_SOFTMAX_TOPK ? topk_gap(lg, E, rp.logit_bias, rp.K, lane) < REFINE_GAP
+                                                         : sg_near_tie(lg, E, rp, REFINE_GAP, lane);
     if (lane == 0 && refine) flag[1 + atomicAdd(flag, 1)] = t;
 }
 

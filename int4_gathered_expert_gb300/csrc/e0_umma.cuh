@@ -41,11 +41,23 @@ E0_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) after `limit_ns` of wall time or as soon as *abort becomes non-zero.
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about `hint_ns` pass, instead of spinning on issue slots
+// the working warps of the SM need
+E0_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 E0_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile uint32_t* abort, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
@@ -88,6 +100,16 @@ E0_DEV void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t i
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulate; A is M rows in
+// M lanes of tensor memory, K-major, two fp16 of consecutive k per 32-bit column
+// (one MMA of K = 16 reads 8 columns).  Issued by one thread.
+E0_DEV void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // arrive (once) on `bar` when every tcgen05.mma issued so far by this thread has completed
 E0_DEV void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -108,6 +130,15 @@ E0_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 E0_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 bits, 32 consecutive columns: thread t of the warp writes
+// TMEM lane (32*(warp%4) + t), columns col..col+31.
+E0_DEV void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+                 : "memory");
+}
+E0_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes (64 fp16) stored in 8-row groups of 1024 bytes (the layout a TMA
@@ -175,6 +206,34 @@ E0_DEV void dequant64_to_tile(const uint4 c0, const uint4 c1, uint32_t sb_bits, 
         out.z = *reinterpret_cast<uint32_t*>(&o2);
         out.w = *reinterpret_cast<uint32_t*>(&o3);
         *reinterpret_cast<uint4*>(rowp + ((k ^ (r & 7)) << 4)) = out;
+    }
+}
+
+// The same dequantisation into registers: o[c] holds k = 2c, 2c + 1 (the
+// column order of a K-major A row in tensor memory).
+E0_DEV void dequant64_to_regs(const uint4 c0, const uint4 c1, uint32_t sb_bits, uint32_t (&o)[32]) {
+    const __half2 sb = *reinterpret_cast<const __half2*>(&sb_bits);
+    const __half2 s2 = __low2half2(sb), b2 = __high2half2(sb);
+    const uint32_t m1024 = 0x64006400u, m64 = 0x54005400u;
+    const __half2 h1024 = *reinterpret_cast<const __half2*>(&m1024);
+    const __half2 h64 = *reinterpret_cast<const __half2*>(&m64);
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t x = w[k], y = x >> 8;
+        uint32_t p0 = lop_and_or(x, 0x000F000Fu, m1024);
+        uint32_t p1 = lop_and_or(x, 0x00F000F0u, m64);
+        uint32_t p2 = lop_and_or(y, 0x000F000Fu, m1024);
+        uint32_t p3 = lop_and_or(y, 0x00F000F0u, m64);
+        __half2 q0 = __hsub2(*reinterpret_cast<__half2*>(&p0), h1024);
+        __half2 q1 = __hsub2(*reinterpret_cast<__half2*>(&p1), h64);
+        __half2 q2 = __hsub2(*reinterpret_cast<__half2*>(&p2), h1024);
+        __half2 q3 = __hsub2(*reinterpret_cast<__half2*>(&p3), h64);
+        __half2 o0 = __hfma2(q0, s2, b2), o1 = __hfma2(q1, s2, b2), o2 = __hfma2(q2, s2, b2), o3 = __hfma2(q3, s2, b2);
+        o[4 * k + 0] = *reinterpret_cast<uint32_t*>(&o0);
+        o[4 * k + 1] = *reinterpret_cast<uint32_t*>(&o1);
+        o[4 * k + 2] = *reinterpret_cast<uint32_t*>(&o2);
+        o[4 * k + 3] = *reinterpret_cast<uint32_t*>(&o3);
     }
 }
 

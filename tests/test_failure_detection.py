@@ -100,16 +100,18 @@ def test_stack_status_clean_on_a_normal_token(L):
 
 @pytest.mark.gpu
 def test_stack_ll_wait_limit_ends_in_timeout_and_recovers(L):
-    """impl 3 with a 1 us wait limit (E0MOE_WAIT_US, read at prepare): the
-    flag-carrying-word polls give up, the launch returns with E0_ST_TIMEOUT in
-    the status word (every block leaves after draining its own bulk copies),
-    and after a prepare with the normal limit the same stack decodes the same
-    bits as a stack that never timed out."""
+    """impl 3 with a 1 us wait limit (E0MOE_WAIT_US, read at prepare): at
+    token 0 every layer routes natively, so each block waits for the gate/up
+    copies it issued right after the routing, longer than 1 us; the launch
+    returns with E0_ST_TIMEOUT in the status word (every block leaves after
+    draining its own bulk copies), and after a prepare with the normal limit
+    the same stack decodes the same bits as a stack that never timed out."""
     _gpu()
+    import dataclasses
     from int4_gathered_expert_gb300 import synth
     from int4_gathered_expert_gb300.model import StackDev
-    shape = synth.StackShape(layer=synth.TINY, n_layers=3, owners=(0, 1), shared_expert=True, seed=9)
-    m = synth.stack_model(shape, n_tokens=2, threads=2)
+    shape = dataclasses.replace(synth.STACK35B, n_layers=6, owners=(1, 2, 3, 4), seed=50)
+    m = synth.stack_model(shape, n_tokens=2)
     X = torch.from_numpy(m.x).cuda()
     ref = StackDev(m, trace=False)
     want = [ref.step(X[t], impl=3).cpu().numpy().copy() for t in range(2)]
@@ -133,3 +135,5 @@ def test_stack_ll_wait_limit_ends_in_timeout_and_recovers(L):
     assert int(sd.status.item()) == 0
     for a, b in zip(got, want):
         assert np.array_equal(a, b)
+    del ref, sd
+    torch.cuda.empty_cache()
