@@ -89,7 +89,7 @@ E0_DEV unsigned long long ll_poll(const unsigned long long* p, uint32_t ep, LLCt
     for (uint32_t it = 1;; ++it) {
         const unsigned long long w = ll_get(p);
         if (ll_ok(w, ep)) return w;
-        if ((it & 31u) == 0) {
+        if ((it & 7u) == 0) {  // each round is an L2 round trip: the clock is read every few
             unsigned ab;
             asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(ab) : "l"(cx.abort_flag) : "memory");
             uint64_t t1;
