@@ -350,13 +350,14 @@ static size_t router_gemm_smem() { return (size_t)STAGES * (BM * BK * 2 + BN * B
 // In the gate/up GEMM a 128-row slice is 64 intermediate rows with the gate
 // and up rows interleaved (the slot layout stores them that way), so each
 // SwiGLU pair sits in adjacent TMEM lanes.
-constexpr int P2_OP_STAGES = 6;
-constexpr int P2_RAW_STAGES = 16;
+constexpr int P2_BK = 128;           // K of one pipeline step (eight MMAs of K = 16)
+constexpr int P2_OP_STAGES = 4;
+constexpr int P2_RAW_STAGES = 8;
 constexpr int P2_THREADS = 480;
 constexpr int P2_BN = 128;
-constexpr uint32_t P2_B = P2_BN * 128;     // token tile
-constexpr uint32_t P2_RAW = 128 * 32;      // raw int4 codes of one K step
-constexpr uint32_t P2_OP = P2_B;           // shared memory of an operand stage
+constexpr uint32_t P2_B = P2_BN * 128;     // token tile of 64 k (one 128B-swizzled TMA box)
+constexpr uint32_t P2_RAW = 128 * P2_BK / 2;  // raw int4 codes of one K step
+constexpr uint32_t P2_OP = 2 * P2_B;       // shared memory of an operand stage: two token tiles
 constexpr uint32_t P2_ACOL = 2 * P2_BN;    // first tensor-memory column of the A tiles (after two accumulators)
 
 struct P2Item {
@@ -404,11 +405,11 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
     // two fp32 accumulators of P2_BN columns, then one 32-column fp16 A tile
     // (128 rows x 64 k) per operand stage
     constexpr uint32_t TMEM_COLS = 512;
-    static_assert(P2_ACOL + 32 * P2_OP_STAGES <= TMEM_COLS, "tensor-memory columns");
+    static_assert(P2_ACOL + (P2_BK / 2) * P2_OP_STAGES <= TMEM_COLS, "tensor-memory columns");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int MT = MODE == MODE_GATEUP ? (2 * p.I) / 128 : p.H / 128;
     const int n_items = *p.n_tiles * MT;
-    const int nk = p.K / BK;
+    const int nk = p.K / P2_BK;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -473,19 +474,26 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             // this group's steps of the item: kk = kk0, kk0 + 2, ...
             const int kk0 = (int)((gbase + (uint32_t)grp) & 1u);
             const int n_own = nk > kk0 ? (nk - kk0 + 1) / 2 : 0;
-            // (scale, bias) words of 8 own steps are loaded one chunk ahead of use
-            uint32_t sbw[8], sbn[8];
+            // (scale, bias) words of 4 own steps (two 64-groups each) are loaded
+            // one chunk ahead of use
+            uint32_t sbw[4][2], sbn[4][2];
 #pragma unroll
-            for (int d = 0; d < 8; ++d) sbn[d] = (ex && d < n_own) ? ldg_u32(sbp + (size_t)(kk0 + 2 * d) * sstep) : 0u;
-            for (int i0 = 0; i0 < n_own && ok; i0 += 8) {
+            for (int d = 0; d < 4; ++d)
 #pragma unroll
-                for (int d = 0; d < 8; ++d) {
-                    sbw[d] = sbn[d];
-                    const int in = i0 + 8 + d;
-                    sbn[d] = (ex && in < n_own) ? ldg_u32(sbp + (size_t)(kk0 + 2 * in) * sstep) : 0u;
+                for (int h = 0; h < 2; ++h)
+                    sbn[d][h] = (ex && d < n_own) ? ldg_u32(sbp + (size_t)(2 * (kk0 + 2 * d) + h) * sstep) : 0u;
+            for (int i0 = 0; i0 < n_own && ok; i0 += 4) {
+#pragma unroll
+                for (int d = 0; d < 4; ++d) {
+                    const int in = i0 + 4 + d;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        sbw[d][h] = sbn[d][h];
+                        sbn[d][h] = (ex && in < n_own) ? ldg_u32(sbp + (size_t)(2 * (kk0 + 2 * in) + h) * sstep) : 0u;
+                    }
                 }
 #pragma unroll
-                for (int d = 0; d < 8; ++d) {
+                for (int d = 0; d < 4; ++d) {
                     const int i = i0 + d;
                     if (i >= n_own) break;
                     const uint32_t g = gbase + (uint32_t)(kk0 + 2 * i);
@@ -499,21 +507,26 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    uint32_t o[32];
-                    if (ex) {
-                        // gate/up raw tile: [128 rows][32 B]; down raw tile: [8 row
-                        // blocks][2 half-groups][16 rows][16 B]
-                        const uint8_t* raw = raw_ring + rs * P2_RAW;
-                        const uint8_t* rd = raw + ((r / DROWS) * 2 * DROWS + r % DROWS) * 16;
-                        const uint4 c0 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 : rd);
-                        const uint4 c1 = *reinterpret_cast<const uint4*>(MODE == MODE_GATEUP ? raw + r * 32 + 16
-                                                                                              : rd + DROWS * 16);
-                        dequant64_to_regs(c0, c1, sbw[d], o);
-                    } else {
+                    // gate/up raw tile: [128 rows][64 B]; down raw tile: [8 row
+                    // blocks][4 half-groups][16 rows][16 B]
+                    const uint8_t* raw = raw_ring + rs * P2_RAW;
+                    const uint8_t* rd = raw + ((r / DROWS) * 4 * DROWS + r % DROWS) * 16;
+                    const uint32_t acol = tmem + ((uint32_t)(q4 * 32) << 16) + P2_ACOL + os * (P2_BK / 2);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) o[c] = 0u;
+                    for (int h = 0; h < 2; ++h) {  // the two 64-input groups of the step
+                        uint32_t o[32];
+                        if (ex) {
+                            const uint4 c0 = *reinterpret_cast<const uint4*>(
+                                MODE == MODE_GATEUP ? raw + r * 64 + h * 32 : rd + 2 * h * DROWS * 16);
+                            const uint4 c1 = *reinterpret_cast<const uint4*>(
+                                MODE == MODE_GATEUP ? raw + r * 64 + h * 32 + 16 : rd + (2 * h + 1) * DROWS * 16);
+                            dequant64_to_regs(c0, c1, sbw[d][h], o);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) o[c] = 0u;
+                        }
+                        tmem_st32(acol + h * 32, o);
                     }
-                    tmem_st32(tmem + ((uint32_t)(q4 * 32) << 16) + P2_ACOL + os * 32, o);
                     tmem_st_wait();
                     tc_fence_before();
                     // once every lane is here, the warp has also used the values it
@@ -589,8 +602,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                     }
                     uint8_t* dst = raw_ring + rs * P2_RAW;
                     mbar_arrive_expect_tx(&raw_full[rs], P2_RAW);
-                    if (MODE == MODE_GATEUP) tma_load_3d(&tmCodes, &raw_full[rs], dst, kk * 32, it.m * 128, z);
-                    else tma_load_5d(&tmCodes, &raw_full[rs], dst, 0, 0, 2 * kk, it.m * (128 / DROWS), z);
+                    if (MODE == MODE_GATEUP) tma_load_3d(&tmCodes, &raw_full[rs], dst, kk * (P2_BK / 2), it.m * 128, z);
+                    else tma_load_5d(&tmCodes, &raw_full[rs], dst, 0, 0, 4 * kk, it.m * (128 / DROWS), z);
                 }
             }
             // the copies issued into each slot have landed before the block leaves
@@ -615,8 +628,9 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                         atomicOr(p.err, 512u);
                         break;
                     }
-                    mbar_arrive_expect_tx(&b_full[os], P2_B);
-                    tma_load_2d(&tmB, &b_full[os], smem + os * P2_OP, kk * BK, it.row0);
+                    mbar_arrive_expect_tx(&b_full[os], 2 * P2_B);
+                    tma_load_2d(&tmB, &b_full[os], smem + os * P2_OP, kk * P2_BK, it.row0);
+                    tma_load_2d(&tmB, &b_full[os], smem + os * P2_OP + P2_B, kk * P2_BK + 64, it.row0);
                 }
             }
             for (uint32_t d = 0; d < P2_OP_STAGES && d < g; ++d) {
@@ -652,11 +666,11 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(smem + os * P2_OP);
-                    const uint32_t a_tm = tmem + P2_ACOL + os * 32;
+                    const uint32_t a_tm = tmem + P2_ACOL + os * (P2_BK / 2);
 #pragma unroll
-                    for (int j = 0; j < BK / 16; ++j)
-                        umma_f16_ta(tmem + buf * P2_BN, a_tm + j * 8, sdesc_k_sw128(b_addr + j * 32), idesc,
-                                    (kk | j) != 0);
+                    for (int j = 0; j < P2_BK / 16; ++j)
+                        umma_f16_ta(tmem + buf * P2_BN, a_tm + j * 8,
+                                    sdesc_k_sw128(b_addr + (j >> 2) * P2_B + (j & 3) * 32), idesc, (kk | j) != 0);
                     umma_commit(&op_empty[os]);
                 }
                 if (!ok) break;
@@ -1003,7 +1017,7 @@ static bool make_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uin
     if (!fn) return false;
     cuuint64_t dims[3] = {inner, rows, slots};
     cuuint64_t strides[2] = {inner, slot_stride};
-    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t box[3] = {64, 128, 1};  // one K step of 128 inputs of 128 rows
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1011,16 +1025,16 @@ static bool make_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uin
 }
 
 // 5-D map over the down codes of every slot, in row blocks: {16 bytes, DROWS
-// rows of a block, I/32 half-groups, H/DROWS blocks, slots}; one box = two
-// half-groups (one 64-input K step) of 128 rows (8 blocks), stored
-// [8][2][DROWS][16 B] in shared memory.
+// rows of a block, I/32 half-groups, H/DROWS blocks, slots}; one box = four
+// half-groups (one 128-input K step) of 128 rows (8 blocks), stored
+// [8][4][DROWS][16 B] in shared memory.
 static bool make_down_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t slots,
                           uint64_t slot_stride) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[5] = {16, DROWS, I / 32, H / DROWS, slots};
     cuuint64_t strides[4] = {16, (cuuint64_t)DROWS * 16, (I / 32) * DROWS * 16, slot_stride};
-    cuuint32_t box[5] = {16, DROWS, 2, 128 / DROWS, 1};
+    cuuint32_t box[5] = {16, DROWS, 4, 128 / DROWS, 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
