@@ -228,16 +228,13 @@ struct LLSmem {
             o = (o + n + 15) & ~(size_t)15;
             return (uint32_t)at;
         };
+        // regions whose size follows from the layer shape alone come first: in
+        // the kernel their offsets are compile-time constants
         hdr = take(sizeof(StackHdr));
-        lyr = take((size_t)L * sizeof(LayerP));
         r = take((size_t)H * 4);
         hpl = take((size_t)GH * 8 * 16);
         hxg = take((size_t)GH * sizeof(XGroup));
         red = take(32 * 4);
-        inds = take((size_t)L * K * 4);
-        w = take((size_t)L * K * 4);
-        prev = take((size_t)L * K * 4);
-        slots = take((size_t)L * (K + 1) * 8);
         tab = take((size_t)E * 4);
         lg = take((size_t)E * 4);
         scr = take((size_t)2 * E * 4);
@@ -248,12 +245,18 @@ struct LLSmem {
         pb2 = take(2 * LL_NW * 4);
         prt = take(LL_MAX_RITEMS * 4);
         pla = take(LL_NW * 4);
-        ghp = take((size_t)(hidden > 0 ? hidden : 1) * 4);
         ypart = take((size_t)2 * LL_NW * LL_MAXROWS * 4);
         zv = take(3 * LL_RANK * 4);
-        aso = take((size_t)g.ma * 4);
         zdp = take((size_t)LL_MAX_SHCTA * LL_RANK * 4);
         bars = take(4 * 8);  // head-side [2], gate/up, down
+        // then those sized by the layer count, the head width and the grid
+        lyr = take((size_t)L * sizeof(LayerP));
+        inds = take((size_t)L * K * 4);
+        w = take((size_t)L * K * 4);
+        prev = take((size_t)L * K * 4);
+        slots = take((size_t)L * (K + 1) * 8);
+        ghp = take((size_t)(hidden > 0 ? hidden : 1) * 4);
+        aso = take((size_t)g.ma * 4);
         // head-side buffer (two, by layer parity): LoRA A row, fc2 rows, B_down rows, router rows
         size_t hb = 0;
         h_la = (uint32_t)hb;
@@ -655,8 +658,8 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
     int pend = -1;  // layer whose head partial sums wait to be published
     // Publish the head sums left by layer lp: fc1 / linear-residual rows of
     // owner lp (hidden and zres words, b1 given per thread), fc2 rows of owner
-    // lp-1 (logit words, with b2 and the zres word of owner lp-1).
-    auto combine = [&](int lp, float b1v, float b2v) {
+    // lp-1 (logit words, with b2 and zrv, the zres word of owner lp-1).
+    auto combine = [&](int lp, float b1v, float b2v, float zrv) {
         const LLPart P = ll_part<C>(lyr, Lz, lp, c, nb);
         const LayerP& L = lyr[lp];
         const int pp = lp & 1;  // partial sums of layer lp (double-buffered: the next layer writes the other half)
@@ -670,8 +673,7 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
         if (P.head_prev && tid >= 32 && tid - 32 < P.F1 - P.F0) {
             const LayerP& O = lyr[lp - 1];
             const int NCF = O.hidden / 256, e0 = tid - 32, e = P.F0 + e0;
-            const unsigned long long* zr = S.llHp + (size_t)((lp - 1) & 1) * (O.hidden + E) + O.hidden;
-            float v = b2v + ll_wait(zr + e, ep0 + lp - 1, cx);
+            float v = b2v + zrv;
             for (int ch = 0; ch < NCF; ++ch) v += pb2[pp * LL_NW + e0 * NCF + ch];
             ll_put(S.llZ + (size_t)(lp - 1) * E + e, v, ep0 + lp);
             if (tr.head_logits) tr.head_logits[(size_t)(lp - 1) * E + e] = v;
@@ -688,6 +690,17 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
             b2h = __ldg(reinterpret_cast<const unsigned short*>(lyr[lp - 1].b2) + P.F0 + tid - 32);
     };
     auto h2f = [](unsigned short h) { return __half2float(__ushort_as_half(h)); };
+    // The zres word of owner lp-1 that this thread's fc2 row adds in
+    // combine(lp) (null: none).  It must be read before this CTA publishes an
+    // a-word of layer lp+1: until then no CTA can finish that layer and rewrite
+    // the word's buffer (owner lp+1's words, two layers on), whether or not
+    // this CTA holds down rows.
+    auto zres_word = [&](int lp) -> const unsigned long long* {
+        const LLPart P = ll_part<C>(lyr, Lz, lp, c, nb);
+        if (!(P.head_prev && tid >= 32 && tid - 32 < P.F1 - P.F0)) return nullptr;
+        const LayerP& O = lyr[lp - 1];
+        return S.llHp + (size_t)((lp - 1) & 1) * (O.hidden + E) + O.hidden + P.F0 + (tid - 32);
+    };
 
     for (int l = lb; l < le; ++l) {
         const LayerP& L = lyr[l];
@@ -706,6 +719,8 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
         const int n_own = P.A1 - P.ps0;  // this CTA's shared-expert a-values
         unsigned short b1h = 0, b2h = 0, adh = 0, ohh = 0;
         int tabv0 = -1, tabv1 = -1;
+        const unsigned long long* zrp = nullptr;  // the zres word of combine(lp)
+        unsigned long long zrw = 0;
         // the one-hot terms of this layer's head rows (lane < 2K of warp q - Q0):
         // this layer's experts, then the previous token's
         auto load_oh = [&]() {
@@ -734,7 +749,11 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
                 if (tid < E) tabv0 = __ldcg(L.table + tid);
                 if (tid + LL_NW * 32 < E) tabv1 = __ldcg(L.table + tid + LL_NW * 32);
             }
-            if (lp >= 0) combine_bias(lp, b1h, b2h);
+            if (lp >= 0) {
+                combine_bias(lp, b1h, b2h);
+                zrp = zres_word(lp);
+                if (zrp) zrw = ll_get(zrp);  // in flight with the residual words below
+            }
             if (P.lora && warp < rank && lane < n_own)
                 adh = __ldg(reinterpret_cast<const unsigned short*>(L.Ad) + (size_t)warp * I + (P.ps0 - P.NAr) + lane);
             if (!native) load_oh();
@@ -784,6 +803,10 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
                 if (tid < E) tab_s[tid] = tabv0;
                 if (tid + LL_NW * 32 < E) tab_s[tid + LL_NW * 32] = tabv1;
             }
+            // the zres word, taken before the barrier below (which precedes every
+            // a-word this CTA publishes in layer l); kept in the z_d gather area,
+            // unused until step 4
+            if (zrp) zdp[tid] = ll_take(zrw, zrp, ep0 + lp - 1, cx);
         }
         // a thread that gave up waiting: the whole block leaves
         if (__syncthreads_or(bad)) {
@@ -859,9 +882,9 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
         const bool la_cta = P.lora && c < 2 * rank;
         float kg0 = 0.f, ku0 = 0.f, kg1 = 0.f, ku1 = 0.f;
         if (cw) {
-            wait_bar(&bars[2], wt_g);
-            // LoRA A rows of the shared expert first: CTA c < 2r takes row c of
-            // [A_gate ; A_up], warps 8..15 one 256-column chunk each
+            // LoRA A rows of the shared expert first (they need only r and the
+            // head-side buffer): CTA c < 2r takes row c of [A_gate ; A_up],
+            // warps 8..15 one 256-column chunk each
             if (la_cta && warp >= 8) {
                 const int ch = warp - 8;
                 float v = 0.f;
@@ -880,6 +903,7 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
                     ll_put(S.llZg + c, z * inv_denom, ep);
                 }
             }
+            wait_bar(&bars[2], wt_g);
             // this CTA's a-values: a = silu(G h) * (U h) -> a-words; a shared-expert
             // row with LoRA keeps its pre-activations for the LoRA terms below
             const int g = lane % G;
@@ -952,7 +976,7 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
         // next layer)
         const int hidp = P.head_prev ? lyr[l - 1].hidden : 0;
         if (cw) {
-            if (lp >= 0) combine(lp, h2f(b1h), h2f(b2h));
+            if (lp >= 0) combine(lp, h2f(b1h), h2f(b2h), zrp ? zdp[tid] : 0.f);
             if (P.head) {
 #pragma unroll
                 for (int m = 0; m < LL_MAXB1; ++m) {
@@ -1078,12 +1102,17 @@ __global__ void __launch_bounds__(LL_THREADS, 1)
     // whose logits were completed in this launch (owners lb-1 .. le-2) into the
     // prediction for the next token
     unsigned short b1h = 0, b2h = 0;
-    if (pend >= 0 && cw) combine_bias(pend, b1h, b2h);
+    float zrv = 0.f;
+    if (pend >= 0 && cw) {
+        combine_bias(pend, b1h, b2h);
+        const unsigned long long* zrp = zres_word(pend);
+        if (zrp) zrv = ll_wait(zrp, ep0 + pend - 1, cx);
+    }
     if (__syncthreads_or(bad)) {
         leave();
         return;
     }
-    if (pend >= 0 && cw) combine(pend, h2f(b1h), h2f(b2h));
+    if (pend >= 0 && cw) combine(pend, h2f(b1h), h2f(b2h), zrv);
     __syncthreads();
     for (int o = max(lb - 1, 0); o <= le - 2; ++o) {
         if (!lyr[o].fc1 || o % nb != c) continue;

@@ -50,3 +50,27 @@ def routing_matches(gpu_inds, gpu_w, rt, allow_tie=True):
             if abs(want[int(e)] - w) > W_ATOL:
                 msgs.append(f"token {t}: weight of expert {e} gpu {w} oracle {want[int(e)]}")
     return exempt, msgs
+
+
+def tile_edge_tokens(inds, n_experts=3, tile=128, per_expert=8):
+    """Tokens that sit at the edges of the token tiles of the ``n_experts``
+    busiest experts: an expert's tokens, in token order (the order a stable
+    sort by expert keeps), are cut into tiles of ``tile``; the first and last
+    token of each tile and the expert's last token are taken, up to
+    ``per_expert`` of them.  Tile-boundary mistakes in a grouped GEMM show up
+    on exactly these tokens."""
+    inds = np.asarray(inds)
+    counts = np.bincount(inds.ravel(), minlength=int(inds.max()) + 1)
+    out = set()
+    for e in np.argsort(-counts, kind="stable")[:n_experts]:
+        toks = np.nonzero((inds == e).any(axis=1))[0]
+        n = len(toks)
+        pos = []
+        for t0 in range(0, n, tile):
+            pos += [t0, min(t0 + tile, n) - 1]
+        pos = sorted(set(pos))
+        if len(pos) > per_expert:
+            keep = np.linspace(0, len(pos) - 1, per_expert).round().astype(int)
+            pos = [pos[i] for i in keep]
+        out.update(int(toks[p]) for p in pos)
+    return sorted(out)

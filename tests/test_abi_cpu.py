@@ -108,3 +108,18 @@ def test_host_validation_of_ranges_prefetch_and_selftest(lib):
     assert lib.e0_selftest_bounded_wait(some, 1000, None, None) == L.E0_ERR_NULL
     assert lib.e0_selftest_bounded_wait(some, 0, some, None) == L.E0_ERR_ARG
     assert lib.e0_selftest_bounded_wait(some, L.E0_SELFTEST_MAX_WAIT_US + 1, some, None) == L.E0_ERR_ARG
+
+
+def test_tile_edge_sampler_covers_every_tile_of_the_busiest_expert():
+    """The parity sampler of the full-size prefill tests: for a hand-made
+    routing where expert 5 takes tokens 0..299 (three 128-token tiles), the
+    tokens picked for it are the first and last of each tile."""
+    import numpy as np
+    from tests.parity import tile_edge_tokens
+    inds = np.zeros((400, 2), np.int32)
+    inds[:300, 0] = 5
+    inds[300:, 0] = 7
+    inds[:, 1] = np.arange(400) % 3
+    inds[:300, 1] = 1 + np.arange(300) % 2  # no token holds expert 5 twice
+    got = tile_edge_tokens(inds, n_experts=1, tile=128, per_expert=8)
+    assert got == [0, 127, 128, 255, 256, 299]

@@ -5,7 +5,7 @@ import pytest
 
 from int4_gathered_expert_gb300 import synth
 from oracle import e0_oracle as O
-from tests.parity import REL_L2, rel_l2, routing_matches
+from tests.parity import REL_L2, rel_l2, routing_matches, tile_edge_tokens
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -120,9 +120,12 @@ def test_35b_prefill_full_size(L, prefill35):
     # expert load is Zipf-like (the workload's recipe)
     counts = np.bincount(inds.ravel(), minlength=s.E)
     assert counts.sum() == T * s.K and counts.max() > 20 * np.median(counts)
-    # outputs on a sample of tokens, including the first and the last
+    # outputs on a sample of tokens: the first and the last, random ones, and
+    # the tokens at the tile edges of the three busiest experts (several
+    # 128-token tiles each)
     g = np.random.default_rng(0)
-    sample = sorted(set([0, T - 1] + g.choice(T, 22, replace=False).tolist()) - set(ex))
+    edges = tile_edge_tokens(inds)
+    sample = sorted(set([0, T - 1] + g.choice(T, 22, replace=False).tolist() + edges) - set(ex))
     Yo = O.moe_block(d["X"][sample].astype(np.float64), O.BankExperts(d["bank"]), rt.inds[sample], rt.w[sample])
     errs = [rel_l2(Y[t], Yo[i]) for i, t in enumerate(sample)]
     assert max(errs) <= REL_L2, max(errs)
@@ -156,7 +159,7 @@ def test_8b_prefill_sigmoid_group(L, prefill8):
     counts = np.bincount(inds.ravel(), minlength=s.E)
     assert counts.sum() == T * s.K
     g = np.random.default_rng(1)
-    sample = sorted(set([0, T - 1] + g.choice(T, 22, replace=False).tolist()) - set(ex))
+    sample = sorted(set([0, T - 1] + g.choice(T, 22, replace=False).tolist() + tile_edge_tokens(inds)) - set(ex))
     Yo = O.moe_block(d["X"][sample].astype(np.float64), O.BankExperts(d["bank"]), rt.inds[sample], rt.w[sample])
     errs = [rel_l2(Y[t], Yo[i]) for i, t in enumerate(sample)]
     assert max(errs) <= REL_L2, max(errs)
