@@ -553,10 +553,17 @@ def peaks():
         return None
 
 
-def kernel_source_digest():
+# the sources each profiled kernel is compiled from (a change to any of them
+# voids its recorded DRAM traffic)
+KERNEL_SOURCES = {
+    "k_stack_ll": ("e0_common.cuh", "e0_decode.cuh", "e0_decode.cu", "e0_internal.h", "e0_stack_ll.cuh"),
+}
+
+
+def kernel_source_digest(kernel: str = "k_stack_ll"):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "int4_gathered_expert_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -569,7 +576,7 @@ def recorded_traffic(kernel: str):
     except (OSError, ValueError):
         return None
     k = rec.get(kernel)
-    if not k or k.get("source_digest") != kernel_source_digest():
+    if not k or kernel not in KERNEL_SOURCES or k.get("source_digest") != kernel_source_digest(kernel):
         return None
     return k.get("dram_bytes_per_launch")
 
