@@ -16,6 +16,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "e0_decode.cuh"
 #include "e0_internal.h"
@@ -399,6 +400,12 @@ E0_DEV void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst, int x,
         : "memory");
 }
 
+// SiLU for the gate/up epilogue, from CUDA's fast exponential and division
+// intrinsics (relative error ~1e-7, far below the fp16 rounding of the
+// result): x * sigmoid(x) = x / (1 + e^-x); for x -> -inf the divisor
+// overflows and the quotient goes to 0, for x -> +inf it is x.
+E0_DEV float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
 template <int MODE>
 __global__ void __launch_bounds__(P2_THREADS, 1)
     k_umma2(const __grid_constant__ CUtensorMap tmCodes, const __grid_constant__ CUtensorMap tmB, GemmP p) {
@@ -556,26 +563,37 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             }
             tc_fence_after();
             const int n_mma = (it.ncount + 15) & ~15;
-            for (int c0 = 0; c0 < n_mma && have; c0 += 16) {
-                float acc[16];
-                tmem_ld16(tq + buf * P2_BN + c0, acc);
+            // per item: the output base of this lane's row; per 32 columns: two
+            // tensor-memory loads, one wait
+            __half* hout = nullptr;
+            float* yout = nullptr;
+            if (MODE == MODE_GATEUP) hout = p.abuf + (size_t)it.row0 * p.I + it.m * 64 + (q >> 1);
+            else yout = p.yp + (size_t)it.row0 * p.H + it.m * 128 + q;
+            for (int c0 = 0; c0 < n_mma && have; c0 += 32) {
+                float acc[32];
+                tmem_ld16(tq + buf * P2_BN + c0, *reinterpret_cast<float(*)[16]>(acc));
+                const bool two = c0 + 16 < n_mma;  // warp-uniform
+                if (two) tmem_ld16(tq + buf * P2_BN + c0 + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
+                else
+#pragma unroll
+                    for (int j = 16; j < 32; ++j) acc[j] = 0.f;
                 tmem_ld_wait();
                 if (MODE == MODE_GATEUP) {
-                    const int i = it.m * 64 + (q >> 1);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 32; ++j) {
                         const float other = __shfl_xor_sync(0xffffffffu, acc[j], 1);
                         const int col = c0 + j;
                         if (!(q & 1) && col < it.ncount)
-                            p.abuf[(size_t)(it.row0 + col) * p.I + i] = __float2half_rn(silu_f(acc[j]) * other);
+                            hout[(size_t)col * p.I] = __float2half_rn(silu_fast(acc[j]) * other);
                     }
                 } else {
-                    const int jrow = it.m * 128 + q;
+                    // the routing weights of these 32 columns, one per lane
+                    const float wl = c0 + lane < it.ncount ? p.wp[it.row0 + c0 + lane] : 0.f;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 32; ++j) {
                         const int col = c0 + j;
-                        if (col < it.ncount)
-                            p.yp[(size_t)(it.row0 + col) * p.H + jrow] = p.wp[it.row0 + col] * acc[j];
+                        const float wj = __shfl_sync(0xffffffffu, wl, j);
+                        if (col < it.ncount) yout[(size_t)col * p.H] = wj * acc[j];
                     }
                 }
             }
@@ -996,8 +1014,44 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// Encoded tensor maps are kept, keyed by everything the encoding reads (the
+// kind of map, base address and sizes), so that a call with the buffers of an
+// earlier one skips the driver's encode: a cached map equals a fresh one.
+struct MapKey {
+    int kind;
+    const void* base;
+    uint64_t a, b, c, d;
+    bool operator==(const MapKey& o) const {
+        return kind == o.kind && base == o.base && a == o.a && b == o.b && c == o.c && d == o.d;
+    }
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+};
+static std::mutex g_map_mu;
+static std::vector<MapEntry> g_maps;  // most recently added last
+constexpr size_t MAP_CACHE = 64;
+
+template <class Encode>
+static bool cached_map(CUtensorMap* m, const MapKey& k, Encode encode) {
+    {
+        std::lock_guard<std::mutex> g(g_map_mu);
+        for (const MapEntry& e : g_maps)
+            if (e.key == k) {
+                *m = e.map;
+                return true;
+            }
+    }
+    if (!encode(m)) return false;
+    std::lock_guard<std::mutex> g(g_map_mu);
+    if (g_maps.size() >= MAP_CACHE) g_maps.erase(g_maps.begin());
+    g_maps.push_back(MapEntry{k, *m});
+    return true;
+}
+
 // 2-D fp16 row-major [rows][inner] tensor, box = 64 elements x box_rows, 128B swizzle
-static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+static bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, rows};
@@ -1011,8 +1065,8 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
 
 // 3-D uint8 [n_slots][rows][inner] view of one code region of every slot;
 // box = 32 bytes x 128 rows x 1 slot, no swizzle (dense 32-byte rows).
-static bool make_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t slots,
-                           uint64_t slot_stride) {
+static bool encode_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t slots,
+                             uint64_t slot_stride) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {inner, rows, slots};
@@ -1028,8 +1082,8 @@ static bool make_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uin
 // rows of a block, I/32 half-groups, H/DROWS blocks, slots}; one box = four
 // half-groups (one 128-input K step) of 128 rows (8 blocks), stored
 // [8][4][DROWS][16 B] in shared memory.
-static bool make_down_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t slots,
-                          uint64_t slot_stride) {
+static bool encode_down_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t slots,
+                            uint64_t slot_stride) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[5] = {16, DROWS, I / 32, H / DROWS, slots};
@@ -1039,6 +1093,21 @@ static bool make_down_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    return cached_map(m, MapKey{0, base, inner, rows, box_rows, 0},
+                      [&](CUtensorMap* o) { return encode_map(o, base, inner, rows, box_rows); });
+}
+static bool make_codes_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t slots,
+                           uint64_t slot_stride) {
+    return cached_map(m, MapKey{1, base, inner, rows, slots, slot_stride},
+                      [&](CUtensorMap* o) { return encode_codes_map(o, base, inner, rows, slots, slot_stride); });
+}
+static bool make_down_map(CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t slots,
+                          uint64_t slot_stride) {
+    return cached_map(m, MapKey{2, base, H, I, slots, slot_stride},
+                      [&](CUtensorMap* o) { return encode_down_map(o, base, H, I, slots, slot_stride); });
 }
 
 static std::once_flag g_prefill_init;

@@ -163,7 +163,12 @@ def _check(name, rc, raise_on_error):
 
 
 def route_params(mode=E0_ROUTE_SOFTMAX_TOPK, K=4, n_groups=1, topk_groups=1, scale=1.0, logit_bias=None):
-    return RouteParams(mode, K, n_groups, topk_groups, scale, ptr(logit_bias))
+    """The routing parameters as the C ABI takes them.  The struct holds only
+    the device address of ``logit_bias``, so it also keeps a reference to the
+    tensor: a temporary passed here stays allocated as long as the struct."""
+    rp = RouteParams(mode, K, n_groups, topk_groups, scale, ptr(logit_bias))
+    rp._logit_bias = logit_bias
+    return rp
 
 
 # ---------------------------------------------------------------- entry points (same names)

@@ -123,3 +123,22 @@ def test_tile_edge_sampler_covers_every_tile_of_the_busiest_expert():
     inds[:300, 1] = 1 + np.arange(300) % 2  # no token holds expert 5 twice
     got = tile_edge_tokens(inds, n_experts=1, tile=128, per_expert=8)
     assert got == [0, 127, 128, 255, 256, 299]
+
+
+def test_route_params_keeps_its_logit_bias_alive():
+    """The routing struct carries the bias tensor's device address; the tensor
+    must live as long as the struct, also when the caller passed a temporary."""
+    import gc
+    import weakref
+    torch = pytest.importorskip("torch")
+    from int4_gathered_expert_gb300 import lib as L
+    bias = torch.arange(16, dtype=torch.float32)
+    ref = weakref.ref(bias)
+    rp = L.route_params(K=2, logit_bias=bias)
+    addr = bias.data_ptr()
+    del bias
+    gc.collect()
+    assert ref() is not None and rp.logit_bias == addr
+    del rp
+    gc.collect()
+    assert ref() is None
