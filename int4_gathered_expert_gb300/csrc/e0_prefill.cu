@@ -50,7 +50,7 @@ struct PrefillWs {
     float* wp;          // [T*K] routing weight per sorted row
     __half* xp;         // [T*K][H] gathered rows
     __half* abuf;       // [T*K][I] SwiGLU activations
-    float* yp;          // [T*K][H] weighted expert outputs
+    __half* yp;         // [T*K][H] weighted expert outputs (fp16)
     size_t bytes;
     int max_tiles;
 };
@@ -83,7 +83,7 @@ static PrefillWs prefill_ws(char* base, int T, int H, int I, int E, int K) {
     w.wp = reinterpret_cast<float*>(take(A * 4));
     w.xp = reinterpret_cast<__half*>(take(A * H * 2));
     w.abuf = reinterpret_cast<__half*>(take(A * I * 2));
-    w.yp = reinterpret_cast<float*>(take(A * H * 4));
+    w.yp = reinterpret_cast<__half*>(take(A * H * 2));
     w.bytes = off + 256;
     return w;
 }
@@ -199,7 +199,7 @@ struct GemmP {
     const int4* tiles;
     const int32_t* n_tiles;
     __half* abuf;
-    float* yp;
+    __half* yp;
     const float* wp;
     uint32_t* err;
     uint32_t* st;
@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             // per item: the output base of this lane's row; per 32 columns: two
             // tensor-memory loads, one wait
             __half* hout = nullptr;
-            float* yout = nullptr;
+            __half* yout = nullptr;
             if (MODE == MODE_GATEUP) hout = p.abuf + (size_t)it.row0 * p.I + it.m * 64 + (q >> 1);
             else yout = p.yp + (size_t)it.row0 * p.H + it.m * 128 + q;
             for (int c0 = 0; c0 < n_mma && have; c0 += 32) {
@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                     for (int j = 0; j < 32; ++j) {
                         const int col = c0 + j;
                         const float wj = __shfl_sync(0xffffffffu, wl, j);
-                        if (col < it.ncount) yout[(size_t)col * p.H] = wj * acc[j];
+                        if (col < it.ncount) yout[(size_t)col * p.H] = __float2half_rn(wj * acc[j]);
                     }
                 }
             }
@@ -979,17 +979,20 @@ __global__ void k_prefill_gather(const __half* X, int H, int K, const int32_t* p
     for (int c = threadIdx.x; c < H / 8; c += blockDim.x) dst[c] = src[c];
 }
 
-// Y[t] = sum_k yp[pos[t*K + k]]  (k = 0..K-1, fixed order)
-__global__ void k_prefill_combine(const float* yp, const int32_t* pos, int T, int K, int H, float* Y) {
+// Y[t] = sum_k yp[pos[t*K + k]]  (k = 0..K-1, fixed order, fp32 sums of the
+// fp16 rows)
+__global__ void k_prefill_combine(const __half* yp, const int32_t* pos, int T, int K, int H, float* Y) {
     const int t = blockIdx.x;
     for (int j = threadIdx.x * 4; j < H; j += blockDim.x * 4) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < K; ++k) {
-            const float4 v = *reinterpret_cast<const float4*>(yp + (size_t)pos[t * K + k] * H + j);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            const uint2 v = *reinterpret_cast<const uint2*>(yp + (size_t)pos[t * K + k] * H + j);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+            acc.x += a.x;
+            acc.y += a.y;
+            acc.z += b.x;
+            acc.w += b.y;
         }
         *reinterpret_cast<float4*>(Y + (size_t)t * H + j) = acc;
     }
