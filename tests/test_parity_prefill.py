@@ -57,6 +57,45 @@ def run_prefill(L, pool, X16, Wr, rp, T):
     return Y.cpu().numpy(), inds.cpu().numpy(), w.cpu().numpy(), L.e0_read_status(st)
 
 
+def test_prefill_repeated_calls_on_changing_buffers(L):
+    """Calls that alternate two input buffers (and a larger token count in
+    between) through one workspace: each call matches the oracle, and a
+    repeated call gives the same bits (the encoded tensor maps are reused
+    only for the buffers they were made for; no state leaks between calls)."""
+    from int4_gathered_expert_gb300.model import SlotPoolDev
+    d1 = synth.tiny_layer(3, T=200)
+    d2 = synth.tiny_layer(4, T=200)
+    d3 = synth.tiny_layer(5, T=390)
+    s = d1["shape"]
+    pool = SlotPoolDev.resident(d1["bank"], s.H, s.I)
+    rp = L.route_params(K=s.K)
+    ws_bytes = L.e0_workspace_size(2, 390, s.H, s.I, s.E, s.K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Wr = dev(d1["router"])
+
+    def call(x):
+        T = x.shape[0]
+        Y = torch.empty((T, s.H), dtype=torch.float32, device="cuda")
+        inds = torch.empty((T, s.K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, s.K), dtype=torch.float32, device="cuda")
+        L.e0_moe_prefill_forward(dev(x), T, pool.desc, Wr, rp, Y, inds, w, ws, ws_bytes, st)
+        return Y.cpu().numpy(), inds.cpu().numpy(), w.cpu().numpy()
+
+    xs = [d["x"].astype(np.float16) for d in (d1, d2, d3)]
+    runs = [call(xs[i]) for i in (0, 1, 2, 0, 1)]
+    assert L.e0_read_status(st) == 0
+    for i, (Y, inds, w) in zip((0, 1, 2, 0, 1), runs):
+        Yo, rt = O.prefill(xs[i], d1["bank"], d1["router"], s)
+        ex, msgs = routing_matches(inds, w, rt)
+        assert not msgs, msgs[:4]
+        errs = [rel_l2(Y[t], Yo[t]) for t in range(xs[i].shape[0]) if t not in ex]
+        assert max(errs) <= REL_L2, max(errs)
+    for a, b in ((runs[0], runs[3]), (runs[1], runs[4])):
+        for u, v in zip(a, b):
+            assert np.array_equal(u, v)
+
+
 @pytest.mark.parametrize("T", [1, 8, 130, 513])
 def test_tiny_prefill(L, T):
     from int4_gathered_expert_gb300.model import SlotPoolDev
