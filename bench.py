@@ -141,7 +141,11 @@ def run_prefill_bench(dev, reps: int = 5, tier: str = "35b"):
     return {"workload": name,
             "value": T / t, "unit": "tok/s", "ms": t * 1e3, "useful_tflops": flops / t / 1e12,
             "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peak, "unit": "TFLOP/s",
-                         "frac": flops / t / 1e12 / peak, "traffic": None,
+                         "frac": flops / t / 1e12 / peak,
+                         # DRAM bytes of one launch of the dominant kernel (the
+                         # gate/up grouped GEMM), 35B tier only
+                         "traffic": recorded_traffic("k_umma2<1>") if tier == "35b" else None,
+                         "traffic_kernel": "k_umma2<1>" if tier == "35b" else None,
                          "peak_source": "MEASURED_PEAKS.json bf16_tflops (measured, fp16 = bf16 rate)"
                          if pk else "fallback"},
             "l2": "flushed (256 MB write) before each timed call",
@@ -577,6 +581,7 @@ def peaks():
 # voids its recorded DRAM traffic)
 KERNEL_SOURCES = {
     "k_stack_ll": ("e0_common.cuh", "e0_decode.cuh", "e0_decode.cu", "e0_internal.h", "e0_stack_ll.cuh"),
+    "k_umma2<1>": ("e0_common.cuh", "e0_decode.cuh", "e0_internal.h", "e0_prefill.cu", "e0_umma.cuh"),
 }
 
 
