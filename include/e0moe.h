@@ -368,6 +368,18 @@ int e0_stack_update_layers(void* ws, const e0_stack_layer* layers, int L, e0_str
 int e0_stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank,
                               uint32_t* d_status, e0_stream_t stream);
 
+/* e0_stack_prefetch_experts for n layers at once: layers[i] into pools[i]
+ * from banks[i] (host arrays of n entries, 0 <= n <= 64, every pool of one H
+ * and I, no pool twice).  One copy launch covers every layer's missing
+ * experts and one commit launch updates every table, instead of two launches
+ * a layer; the result is that of n calls of e0_stack_prefetch_experts.
+ * Errors: a NULL array or bank -> E0_ERR_NULL; n out of range, a layer out of
+ * range, pools of different H / I or a pool given twice -> E0_ERR_ARG; a
+ * pool failing e0_slot_update's checks -> its code. */
+int e0_stack_prefetch_experts_batch(void* ws, const int32_t* layers, int n, int t_next,
+                                    const e0_slot_pool* pools, const uint8_t* const* banks,
+                                    uint32_t* d_status, e0_stream_t stream);
+
 /* A cross-layer cache of expert bundles in device memory, least recently used
  * first out ([PTKR] "SSD 전문가 스트리밍" / P2 `SharedExpertCache`: a hot set
  * shared by all layers; misses go to the exact path, here the host bank).

@@ -152,6 +152,68 @@ __global__ void k_slot_commit(int32_t* table, int32_t* occupant, int n_slots, in
     if (P.status) set_status(st, P.status);
 }
 
+// Several layers' slot updates in two launches: the copy kernel's blocks come
+// in groups of `per`, group i updating layer i's pool (each block plans its
+// layer's copies itself, as k_slot_copy does); the commit kernel has one block
+// per layer.
+struct PrefetchLayer {
+    int32_t* table;
+    int32_t* occupant;
+    uint8_t* data;
+    const uint8_t* bank;
+    const int32_t* next;
+    int32_t n_slots, E;
+};
+constexpr int PREFETCH_MAX_LAYERS = 64;
+struct PrefetchBatch {
+    PrefetchLayer l[PREFETCH_MAX_LAYERS];
+    int32_t n, K, per;
+    uint64_t sbytes;
+};
+
+__global__ void k_slot_copy_batch(const __grid_constant__ PrefetchBatch B) {
+    __shared__ SlotPlan P;
+    __shared__ uint32_t prot[E0_MAX_E / 32];
+    const int li = blockIdx.x / B.per, b = blockIdx.x % B.per;
+    const PrefetchLayer& L = B.l[li];
+    if (threadIdx.x == 0) slot_plan(L.table, L.occupant, L.n_slots, L.E, L.next, B.K, nullptr, 0, &P, prot);
+    __syncthreads();
+    const size_t chunks = B.sbytes / 16;
+    const size_t total = chunks * P.n;
+    // four 16-byte loads in flight per thread (the bank may be host memory)
+    const size_t stride = (size_t)B.per * blockDim.x;
+    for (size_t q0 = (size_t)b * blockDim.x + threadIdx.x; q0 < total; q0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            if (q < total)
+                v[u] = *reinterpret_cast<const uint4*>(L.bank + (size_t)P.e[q / chunks] * B.sbytes + (q % chunks) * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            if (q < total) *reinterpret_cast<uint4*>(L.data + (size_t)P.s[q / chunks] * B.sbytes + (q % chunks) * 16) = v[u];
+        }
+    }
+}
+
+__global__ void k_slot_commit_batch(const __grid_constant__ PrefetchBatch B, uint32_t* st) {
+    __shared__ SlotPlan P;
+    __shared__ uint32_t prot[E0_MAX_E / 32];
+    if (threadIdx.x != 0) return;
+    const PrefetchLayer& L = B.l[blockIdx.x];
+    slot_plan(L.table, L.occupant, L.n_slots, L.E, L.next, B.K, nullptr, 0, &P, prot);
+    for (int c = 0; c < P.n; ++c) {
+        const int s2 = P.s[c], e = P.e[c];
+        const int old = L.occupant[s2];
+        if (old >= 0 && old < L.E && L.table[old] == s2) L.table[old] = -1;
+        L.occupant[s2] = e;
+        L.table[e] = s2;
+    }
+    if (P.status) set_status(st, P.status);
+}
+
 // ================================================================== cross-layer expert cache
 
 // Plan layout in cache->scratch: [0] n copies, then per copy i (4 ints at
@@ -1216,6 +1278,39 @@ int stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* 
     if (layer < 0 || layer >= hdr.L || t_next < 1) return E0_ERR_ARG;
     const int32_t* next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
     return slot_update(pool, next, hdr.K, nullptr, 0, bank, st, s, hdr.free_sms);
+}
+
+int stack_prefetch_experts_batch(void* ws, const int32_t* layers, int n, int t_next, const e0_slot_pool* pools,
+                                 const uint8_t* const* banks, uint32_t* st, cudaStream_t s) {
+    StackHdr hdr;
+    if (!stack_hdr(ws, &hdr)) return E0_ERR_ARG;
+    if (n < 0 || n > PREFETCH_MAX_LAYERS || t_next < 1) return E0_ERR_ARG;
+    if (n == 0) return E0_OK;
+    PrefetchBatch B;
+    memset(&B, 0, sizeof(B));
+    B.n = n;
+    B.K = hdr.K;
+    for (int i = 0; i < n; ++i) {
+        const int layer = layers[i];
+        if (layer < 0 || layer >= hdr.L) return E0_ERR_ARG;
+        if (pools[i].H != pools[0].H || pools[i].I != pools[0].I) return E0_ERR_ARG;
+        PrefetchLayer& L = B.l[i];
+        L.table = pools[i].slot_table;
+        L.occupant = pools[i].occupant;
+        L.data = pools[i].data;
+        L.bank = banks[i];
+        L.next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
+        L.n_slots = pools[i].n_slots;
+        L.E = pools[i].E;
+    }
+    B.sbytes = slot_bytes(pools[0].H, pools[0].I);
+    // four 512-thread blocks per SM the copies may use, shared out over the layers
+    const int blocks = (hdr.free_sms > 0 ? hdr.free_sms : num_sms()) * 4;
+    B.per = blocks / n > 1 ? blocks / n : 1;
+    k_slot_copy_batch<<<n * B.per, 512, 0, s>>>(B);
+    if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+    k_slot_commit_batch<<<n, 32, 0, s>>>(B, st);
+    return launch_ok();
 }
 
 int stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot_pool* p, const uint8_t* bank,

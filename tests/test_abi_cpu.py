@@ -142,3 +142,26 @@ def test_route_params_keeps_its_logit_bias_alive():
     del rp
     gc.collect()
     assert ref() is None
+
+
+def test_host_validation_of_batched_prefetch(lib):
+    """The batched host-tier prefetch rejects null arrays, null banks and
+    workspaces no stack was prepared in before any launch."""
+    from int4_gathered_expert_gb300 import lib as L
+    unknown = C.c_void_p(256)   # never passed to e0_stack_prepare
+    pools = (L.SlotPool * 2)(L.SlotPool(16, 16, 16, 8, 2048, 512, 256), L.SlotPool(32, 32, 32, 8, 2048, 512, 256))
+    layers = (C.c_int32 * 2)(7, 8)
+    banks = (C.c_void_p * 2)(512, 1024)
+    nobank = (C.c_void_p * 2)(512, None)
+    f = lib.e0_stack_prefetch_experts_batch
+    assert f(None, layers, 2, 1, pools, banks, None, None) == L.E0_ERR_NULL
+    assert f(unknown, None, 2, 1, pools, banks, None, None) == L.E0_ERR_NULL
+    assert f(unknown, layers, 2, 1, None, banks, None, None) == L.E0_ERR_NULL
+    assert f(unknown, layers, 2, 1, pools, None, None, None) == L.E0_ERR_NULL
+    assert f(unknown, layers, 2, 1, pools, banks, None, None) == L.E0_ERR_ARG
+    assert f(unknown, None, 0, 1, None, None, None, None) == L.E0_ERR_ARG   # no stack there, even for n = 0
+    # the binding marshals Python lists into the same call
+    # a null bank is caught per entry, after the workspace is known
+    assert f(unknown, layers, 2, 1, pools, nobank, None, None) == L.E0_ERR_ARG
+    assert L.e0_stack_prefetch_experts_batch(256, [7, 8], 1, list(pools), [512, 1024], stream=0,
+                                             raise_on_error=False) == L.E0_ERR_ARG
