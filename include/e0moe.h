@@ -398,12 +398,27 @@ typedef struct e0_expert_cache {
 /* e0_stack_prefetch_experts with a cross-layer cache in front of `bank`: a
  * predicted expert missing from the layer's pool is copied from its cache
  * entry when it has one (device to device), else from `bank` — and then also
- * into the least recently used cache entry.  Hits, misses and evictions are
+ * into the least recently used cache entry not used by this call (with none
+ * left, the expert is not cached).  Hits, misses and evictions are
  * counted in cache->counters.  Errors as e0_stack_prefetch_experts; a layer
  * * E key beyond n_keys -> E0_ERR_ARG. */
 int e0_stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot_pool* pool,
                                      const uint8_t* bank, const e0_expert_cache* cache,
                                      uint32_t* d_status, e0_stream_t stream);
+
+/* e0_stack_prefetch_experts_cached for n layers at once, with the arrays and
+ * limits of e0_stack_prefetch_experts_batch: one launch plans every layer in
+ * order (the cache's recency order is that of n calls in the order given),
+ * one copies, one commits.  An entry used by one layer of the batch (as a
+ * source or filled) is not evicted for another layer of the same batch; with
+ * every entry so taken, an expert is copied from its bank without being
+ * cached.  The plans live in the stack workspace (cache->scratch is not used).
+ * Errors as e0_stack_prefetch_experts_batch and
+ * e0_stack_prefetch_experts_cached. */
+int e0_stack_prefetch_experts_cached_batch(void* ws, const int32_t* layers, int n, int t_next,
+                                           const e0_slot_pool* pools, const uint8_t* const* banks,
+                                           const e0_expert_cache* cache, uint32_t* d_status,
+                                           e0_stream_t stream);
 
 /* ---- whole-layer prefill (sorted gather + tcgen05 grouped GEMM) ------- */
 

@@ -275,6 +275,24 @@ int e0_stack_prefetch_experts_batch(void* ws, const int32_t* layers, int n, int 
     return e0::stack_prefetch_experts_batch(ws, layers, n, t_next, pools, banks, d_status, cs(stream));
 }
 
+int e0_stack_prefetch_experts_cached_batch(void* ws, const int32_t* layers, int n, int t_next,
+                                           const e0_slot_pool* pools, const uint8_t* const* banks,
+                                           const e0_expert_cache* cache, uint32_t* d_status, e0_stream_t stream) {
+    if (!ws || !cache || (n > 0 && (!layers || !pools || !banks))) return E0_ERR_NULL;
+    if (!e0::stack_known(ws)) return E0_ERR_ARG;
+    if (cache->capacity < 0 || cache->n_keys < 1) return E0_ERR_ARG;
+    if (!cache->key || !cache->stamp || !cache->map || !cache->counters || (cache->capacity > 0 && !cache->data))
+        return E0_ERR_NULL;
+    for (int i = 0; i < n; ++i) {
+        if (!banks[i]) return E0_ERR_NULL;
+        const int rc = check_pool(&pools[i]);
+        if (rc != E0_OK) return rc;
+        for (int j = 0; j < i; ++j)
+            if (pools[j].data == pools[i].data || pools[j].slot_table == pools[i].slot_table) return E0_ERR_ARG;
+    }
+    return e0::stack_prefetch_experts_cached_batch(ws, layers, n, t_next, pools, banks, cache, d_status, cs(stream));
+}
+
 int e0_stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank,
                                      const e0_expert_cache* cache, uint32_t* d_status, e0_stream_t stream) {
     if (!ws || !pool || !bank || !cache) return E0_ERR_NULL;

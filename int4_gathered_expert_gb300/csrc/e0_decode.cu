@@ -162,7 +162,7 @@ struct PrefetchLayer {
     uint8_t* data;
     const uint8_t* bank;
     const int32_t* next;
-    int32_t n_slots, E;
+    int32_t n_slots, E, layer, pad;
 };
 constexpr int PREFETCH_MAX_LAYERS = 64;
 struct PrefetchBatch {
@@ -216,20 +216,21 @@ __global__ void k_slot_commit_batch(const __grid_constant__ PrefetchBatch B, uin
 
 // ================================================================== cross-layer expert cache
 
-// Plan layout in cache->scratch: [0] n copies, then per copy i (4 ints at
-// 4 + 4 i): expert, slot, source entry (-1: the bank), cache entry to fill
-// (-1: none).  One thread plans and updates the cache bookkeeping; the copy
-// kernel and the commit follow in stream order.
-__global__ void k_cache_plan(const int32_t* table, const int32_t* occupant, int n_slots, int E, const int32_t* next,
-                             int n_next, int layer, e0_expert_cache c) {
-    __shared__ SlotPlan P;
-    __shared__ uint32_t prot[E0_MAX_E / 32];
-    const int lane = threadIdx.x & 31;
-    if (threadIdx.x >= 32) return;
+// A plan: [0] n copies, then per copy i (4 ints at 4 + 4 i): expert, slot,
+// source entry (-1: the bank), cache entry to fill (-1: none).
+constexpr int CACHE_PLAN_INTS = 4 + 4 * E0_MAX_K;
+
+// One layer's copies through the cache, planned by one warp (lane 0 keeps the
+// bookkeeping).  Entries stamped after `fresh` were used earlier in the same
+// launch (as a source or as a fill) and are never evicted: the copies of one
+// launch run at the same time, so an entry one of them reads or writes must
+// not become another's target.  With every entry taken the expert is copied
+// from the bank without being cached.
+E0_DEV void cache_plan_layer(const int32_t* table, const int32_t* occupant, int n_slots, int E, const int32_t* next,
+                             int n_next, int layer, const e0_expert_cache& c, int32_t* plan, uint32_t& clock,
+                             uint32_t fresh, SlotPlan& P, uint32_t* prot, int lane) {
     if (lane == 0) slot_plan(table, occupant, n_slots, E, next, n_next, nullptr, 0, &P, prot);
     __syncwarp();
-    int32_t* plan = c.scratch;
-    uint32_t clock = c.counters[0];
     int n = 0;
     for (int i = 0; i < P.n; ++i) {
         const int key = layer * E + P.e[i];
@@ -244,15 +245,18 @@ __global__ void k_cache_plan(const int32_t* table, const int32_t* occupant, int 
         } else {
             if (lane == 0) c.counters[2] += 1;
             if (c.capacity > 0 && key >= 0 && key < c.n_keys) {
-                // least recently used entry (an empty one first: stamp 0), the
-                // warp scanning a strided share each, ties to the lower entry
+                // least recently used entry not used in this launch (an empty
+                // one first: stamp 0), the warp scanning a strided share each,
+                // ties to the lower entry
                 uint32_t best = 0xffffffffu;
                 int bi = 0x7fffffff;
-                for (int j = lane; j < c.capacity; j += 32)
-                    if (c.stamp[j] < best) {
-                        best = c.stamp[j];
+                for (int j = lane; j < c.capacity; j += 32) {
+                    const uint32_t sj = c.stamp[j];
+                    if (sj <= fresh && sj < best) {
+                        best = sj;
                         bi = j;
                     }
+                }
 #pragma unroll
                 for (int o = 16; o; o >>= 1) {
                     const uint32_t ob = __shfl_xor_sync(0xffffffffu, best, o);
@@ -262,16 +266,18 @@ __global__ void k_cache_plan(const int32_t* table, const int32_t* occupant, int 
                         bi = oi;
                     }
                 }
-                fill = bi;
-                if (lane == 0) {
-                    const int old = c.key[fill];
-                    if (old >= 0 && old < c.n_keys) {
-                        c.map[old] = -1;
-                        c.counters[3] += 1;
+                if (bi < c.capacity) {
+                    fill = bi;
+                    if (lane == 0) {
+                        const int old = c.key[fill];
+                        if (old >= 0 && old < c.n_keys) {
+                            c.map[old] = -1;
+                            c.counters[3] += 1;
+                        }
+                        c.key[fill] = key;
+                        c.map[key] = fill;
+                        c.stamp[fill] = ++clock;
                     }
-                    c.key[fill] = key;
-                    c.map[key] = fill;
-                    c.stamp[fill] = ++clock;
                 }
                 __syncwarp();
             }
@@ -285,10 +291,21 @@ __global__ void k_cache_plan(const int32_t* table, const int32_t* occupant, int 
         ++n;
         __syncwarp();  // lane 0's bookkeeping is seen by every lane's next scan
     }
-    if (lane == 0) {
-        plan[0] = n;
-        c.counters[0] = clock;
-    }
+    if (lane == 0) plan[0] = n;
+}
+
+// One layer's plan into cache->scratch; the copy kernel and the commit
+// follow in stream order.
+__global__ void k_cache_plan(const int32_t* table, const int32_t* occupant, int n_slots, int E, const int32_t* next,
+                             int n_next, int layer, e0_expert_cache c) {
+    __shared__ SlotPlan P;
+    __shared__ uint32_t prot[E0_MAX_E / 32];
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x >= 32) return;
+    uint32_t clock = c.counters[0];
+    const uint32_t fresh = clock;
+    cache_plan_layer(table, occupant, n_slots, E, next, n_next, layer, c, c.scratch, clock, fresh, P, prot, lane);
+    if (lane == 0) c.counters[0] = clock;
 }
 
 __global__ void k_cache_copy(uint8_t* pool, const uint8_t* bank, e0_expert_cache c, size_t sbytes) {
@@ -318,6 +335,60 @@ __global__ void k_cache_copy(uint8_t* pool, const uint8_t* bank, e0_expert_cache
                 const size_t off = (q % chunks) * 16;
                 const int s = plan[4 + 4 * i + 1], fill = plan[4 + 4 * i + 3];
                 *reinterpret_cast<uint4*>(pool + (size_t)s * sbytes + off) = v[u];
+                if (fill >= 0) *reinterpret_cast<uint4*>(c.data + (size_t)fill * sbytes + off) = v[u];
+            }
+        }
+    }
+}
+
+// Every layer of a batch planned in order by one warp (one clock, so that no
+// copy of the batch evicts an entry another one uses); plans at plans + i *
+// CACHE_PLAN_INTS.
+__global__ void k_cache_plan_batch(const __grid_constant__ PrefetchBatch B, e0_expert_cache c, int32_t* plans) {
+    __shared__ SlotPlan P;
+    __shared__ uint32_t prot[E0_MAX_E / 32];
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x >= 32) return;
+    uint32_t clock = c.counters[0];
+    const uint32_t fresh = clock;
+    for (int i = 0; i < B.n; ++i) {
+        const PrefetchLayer& L = B.l[i];
+        cache_plan_layer(L.table, L.occupant, L.n_slots, L.E, L.next, B.K, L.layer, c, plans + (size_t)i * CACHE_PLAN_INTS,
+                         clock, fresh, P, prot, lane);
+        __syncwarp();
+    }
+    if (lane == 0) c.counters[0] = clock;
+}
+
+// The batch's copies: block group i carries out layer i's plan.
+__global__ void k_cache_copy_batch(const __grid_constant__ PrefetchBatch B, e0_expert_cache c, const int32_t* plans) {
+    const int li = blockIdx.x / B.per, b = blockIdx.x % B.per;
+    const PrefetchLayer& L = B.l[li];
+    const int32_t* plan = plans + (size_t)li * CACHE_PLAN_INTS;
+    const int n = plan[0];
+    const size_t sbytes = B.sbytes, chunks = sbytes / 16;
+    const size_t total = chunks * (size_t)n;
+    const size_t stride = (size_t)B.per * blockDim.x;
+    for (size_t q0 = (size_t)b * blockDim.x + threadIdx.x; q0 < total; q0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            if (q < total) {
+                const int i = (int)(q / chunks);
+                const int e = plan[4 + 4 * i], src = plan[4 + 4 * i + 2];
+                const uint8_t* from = src >= 0 ? c.data + (size_t)src * sbytes : L.bank + (size_t)e * sbytes;
+                v[u] = *reinterpret_cast<const uint4*>(from + (q % chunks) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            if (q < total) {
+                const int i = (int)(q / chunks);
+                const size_t off = (q % chunks) * 16;
+                const int s2 = plan[4 + 4 * i + 1], fill = plan[4 + 4 * i + 3];
+                *reinterpret_cast<uint4*>(L.data + (size_t)s2 * sbytes + off) = v[u];
                 if (fill >= 0) *reinterpret_cast<uint4*>(c.data + (size_t)fill * sbytes + off) = v[u];
             }
         }
@@ -392,6 +463,7 @@ struct StackHdr {
     unsigned long long ll_wait_ns;  // a poll gives up after this much device time
     int32_t grid3, smem3, pf_dist, ll_ok;
     int32_t free_sms;  // SMs impl 3 leaves to other streams; the prefetch copies run on that many CTAs
+    int32_t* pf_plans;  // [64][4 + 4 E0_MAX_K] plans of a batched prefetch through an expert cache
 };
 
 struct TraceP {
@@ -441,7 +513,9 @@ static size_t stack_layout(StackHdr* hdr, char* base, int L, int H, int I, int E
     unsigned long long* llZ = c.take<unsigned long long>((size_t)L * E);
     unsigned long long* llZg = c.take<unsigned long long>(2 * 16);
     unsigned long long* llZd = c.take<unsigned long long>((size_t)64 * 16);
+    int32_t* pf_plans = c.take<int32_t>((size_t)PREFETCH_MAX_LAYERS * CACHE_PLAN_INTS);
     if (hdr) {
+        hdr->pf_plans = pf_plans;
         hdr->llZg = llZg;
         hdr->llZd = llZd;
         hdr->llR = llR;
@@ -1302,12 +1376,50 @@ int stack_prefetch_experts_batch(void* ws, const int32_t* layers, int n, int t_n
         L.next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
         L.n_slots = pools[i].n_slots;
         L.E = pools[i].E;
+        L.layer = layer;
     }
     B.sbytes = slot_bytes(pools[0].H, pools[0].I);
     // four 512-thread blocks per SM the copies may use, shared out over the layers
     const int blocks = (hdr.free_sms > 0 ? hdr.free_sms : num_sms()) * 4;
     B.per = blocks / n > 1 ? blocks / n : 1;
     k_slot_copy_batch<<<n * B.per, 512, 0, s>>>(B);
+    if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+    k_slot_commit_batch<<<n, 32, 0, s>>>(B, st);
+    return launch_ok();
+}
+
+int stack_prefetch_experts_cached_batch(void* ws, const int32_t* layers, int n, int t_next, const e0_slot_pool* pools,
+                                        const uint8_t* const* banks, const e0_expert_cache* c, uint32_t* st,
+                                        cudaStream_t s) {
+    StackHdr hdr;
+    if (!stack_hdr(ws, &hdr)) return E0_ERR_ARG;
+    if (n < 0 || n > PREFETCH_MAX_LAYERS || t_next < 1) return E0_ERR_ARG;
+    if (n == 0) return E0_OK;
+    PrefetchBatch B;
+    memset(&B, 0, sizeof(B));
+    B.n = n;
+    B.K = hdr.K;
+    for (int i = 0; i < n; ++i) {
+        const int layer = layers[i];
+        if (layer < 0 || layer >= hdr.L) return E0_ERR_ARG;
+        if (pools[i].H != pools[0].H || pools[i].I != pools[0].I) return E0_ERR_ARG;
+        if ((long)(layer + 1) * pools[i].E > c->n_keys) return E0_ERR_ARG;
+        PrefetchLayer& L = B.l[i];
+        L.table = pools[i].slot_table;
+        L.occupant = pools[i].occupant;
+        L.data = pools[i].data;
+        L.bank = banks[i];
+        L.next = hdr.pred_inds + ((size_t)(t_next & 1) * hdr.L + layer) * hdr.K;
+        L.n_slots = pools[i].n_slots;
+        L.E = pools[i].E;
+        L.layer = layer;
+    }
+    B.sbytes = slot_bytes(pools[0].H, pools[0].I);
+    const int blocks = (hdr.free_sms > 0 ? hdr.free_sms : num_sms()) * 4;
+    B.per = blocks / n > 1 ? blocks / n : 1;
+    k_cache_plan_batch<<<1, 32, 0, s>>>(B, *c, hdr.pf_plans);
+    if (launch_ok() != E0_OK) return E0_ERR_CUDA;
+    k_cache_copy_batch<<<n * B.per, 512, 0, s>>>(B, *c, hdr.pf_plans);
     if (launch_ok() != E0_OK) return E0_ERR_CUDA;
     k_slot_commit_batch<<<n, 32, 0, s>>>(B, st);
     return launch_ok();

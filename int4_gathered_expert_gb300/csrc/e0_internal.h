@@ -23,6 +23,9 @@ int stack_prefetch_experts(void* ws, int layer, int t_next, const e0_slot_pool* 
                            cudaStream_t s);
 int stack_prefetch_experts_batch(void* ws, const int32_t* layers, int n, int t_next, const e0_slot_pool* pools,
                                  const uint8_t* const* banks, uint32_t* st, cudaStream_t s);
+int stack_prefetch_experts_cached_batch(void* ws, const int32_t* layers, int n, int t_next, const e0_slot_pool* pools,
+                                        const uint8_t* const* banks, const e0_expert_cache* c, uint32_t* st,
+                                        cudaStream_t s);
 int stack_prefetch_experts_cached(void* ws, int layer, int t_next, const e0_slot_pool* pool, const uint8_t* bank,
                                   const e0_expert_cache* cache, uint32_t* st, cudaStream_t s);
 int route(const float* logits, int T, int E, const e0_route_params* rp, int32_t* inds, float* w, uint32_t* st,

@@ -104,6 +104,8 @@ def load() -> C.CDLL:
         "e0_stack_prefetch_experts_batch": (C.c_int, [vp, P(i32), C.c_int, C.c_int, P(SlotPool), P(vp), vp, vp]),
         "e0_stack_prefetch_experts_cached": (C.c_int, [vp, C.c_int, C.c_int, P(SlotPool), vp, P(ExpertCache), vp,
                                                        vp]),
+        "e0_stack_prefetch_experts_cached_batch": (C.c_int, [vp, P(i32), C.c_int, C.c_int, P(SlotPool), P(vp),
+                                                             P(ExpertCache), vp, vp]),
         "e0_prefill_sort": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, vp, vp, vp, vp, sz, vp]),
         "e0_moe_prefill_forward": (C.c_int, [vp, C.c_int, P(SlotPool), vp, P(RouteParams), vp, vp, vp,
                                              vp, sz, vp, vp]),
@@ -126,7 +128,7 @@ def exported_symbols():
             "e0_prerouter_forward",
             "e0_stack_workspace_size", "e0_stack_prepare", "e0_stack_step", "e0_stack_step_range",
             "e0_stack_update_layers", "e0_stack_prefetch_experts", "e0_stack_prefetch_experts_batch",
-            "e0_stack_prefetch_experts_cached",
+            "e0_stack_prefetch_experts_cached", "e0_stack_prefetch_experts_cached_batch",
             "e0_prefill_sort",
             "e0_moe_prefill_forward", "e0_selftest_bounded_wait", "e0_read_status", "e0_status_string"]
 
@@ -283,6 +285,17 @@ def e0_stack_prefetch_experts_batch(ws, layers, t_next, pools, banks, status=Non
     ba = (vp * max(n, 1))(*[ptr(b) for b in banks])
     rc = load().e0_stack_prefetch_experts_batch(ptr(ws), la, n, int(t_next), pa, ba, ptr(status), stream_handle(stream))
     return _check("e0_stack_prefetch_experts_batch", rc, raise_on_error)
+
+
+def e0_stack_prefetch_experts_cached_batch(ws, layers, t_next, pools, banks, cache, status=None, stream=None,
+                                           raise_on_error=True):
+    n = len(layers)
+    la = (i32 * max(n, 1))(*[int(l) for l in layers])
+    pa = (SlotPool * max(n, 1))(*pools)
+    ba = (vp * max(n, 1))(*[ptr(b) for b in banks])
+    rc = load().e0_stack_prefetch_experts_cached_batch(ptr(ws), la, n, int(t_next), pa, ba, C.byref(cache), ptr(status),
+                                                       stream_handle(stream))
+    return _check("e0_stack_prefetch_experts_cached_batch", rc, raise_on_error)
 
 
 def e0_stack_prefetch_experts(ws, layer, t_next, pool: SlotPool, bank, status=None, stream=None, raise_on_error=True):

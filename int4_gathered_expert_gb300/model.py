@@ -248,14 +248,14 @@ class StreamedStack:
         return L.e0_slot_bytes(self.sd.H, self.sd.I)
 
     def _prefetch(self, layers, t_next, stream):
+        # every layer of the batch in one copy launch and one commit launch
+        pools = [self.pools[l].desc for l in layers]
+        banks = [self.host[l] for l in layers]
         if self.cache is None:
-            # every layer of the batch in one copy launch and one commit launch
-            L.e0_stack_prefetch_experts_batch(self.sd.ws, layers, t_next, [self.pools[l].desc for l in layers],
-                                              [self.host[l] for l in layers], self.status, stream=stream)
-            return
-        for l in layers:
-            L.e0_stack_prefetch_experts_cached(self.sd.ws, l, t_next, self.pools[l].desc, self.host[l],
-                                               self.cache.desc, self.status, stream=stream)
+            L.e0_stack_prefetch_experts_batch(self.sd.ws, layers, t_next, pools, banks, self.status, stream=stream)
+        else:
+            L.e0_stack_prefetch_experts_cached_batch(self.sd.ws, layers, t_next, pools, banks, self.cache.desc,
+                                                     self.status, stream=stream)
 
     def start(self, x0: torch.Tensor, out: Optional[torch.Tensor] = None):
         """Token 0 (every layer routes natively) from the resident bank, then the

@@ -165,3 +165,8 @@ def test_host_validation_of_batched_prefetch(lib):
     assert f(unknown, layers, 2, 1, pools, nobank, None, None) == L.E0_ERR_ARG
     assert L.e0_stack_prefetch_experts_batch(256, [7, 8], 1, list(pools), [512, 1024], stream=0,
                                              raise_on_error=False) == L.E0_ERR_ARG
+    g = lib.e0_stack_prefetch_experts_cached_batch
+    cache = L.ExpertCache()
+    assert g(unknown, layers, 2, 1, pools, banks, None, None, None) == L.E0_ERR_NULL
+    assert g(None, layers, 2, 1, pools, banks, C.byref(cache), None, None) == L.E0_ERR_NULL
+    assert g(unknown, layers, 2, 1, pools, banks, C.byref(cache), None, None) == L.E0_ERR_ARG
