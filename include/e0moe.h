@@ -432,8 +432,11 @@ int e0_prefill_sort(const int32_t* inds, int T, int K, int E, int32_t* counts, i
 /* Prefill one layer for T tokens: route every token natively (logits =
  * W_router X + rp->logit_bias), sort assignments by expert, gather X rows,
  * run gate/up and down as grouped GEMMs on the tensor cores (fp16 operands,
- * weights dequantised on chip, fp32 accumulation), and combine Y[t] =
- * sum_k w[t][k] expert(X[t]) in a fixed order.  X fp16 [T][H]; bank = the
+ * weights dequantised on chip, fp32 accumulation), and form Y[t] =
+ * sum_k w[t][k] expert(X[t]): added in fp32 with atomics (the order of the K
+ * terms varies between runs), or, with the environment variable
+ * E0MOE_PREFILL_FIXED_ORDER=1 at the call, summed from fp16 rows in a fixed
+ * order (the same bits on every run).  X fp16 [T][H]; bank = the
  * layer's experts (slot table consulted per expert); Y fp32 [T][H];
  * inds_out/w_out [T][K].  Prefill never predicts ([JAEHUN] "작동 원리"). */
 int e0_moe_prefill_forward(const uint16_t* X, int T, const e0_slot_pool* bank,

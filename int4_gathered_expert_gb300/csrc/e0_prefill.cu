@@ -13,6 +13,7 @@
 //   7. combine: Y[t] = sum over k (fixed order) of the token's K rows.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -201,6 +202,10 @@ struct GemmP {
     __half* abuf;
     __half* yp;
     const float* wp;
+    const int32_t* perm;   // sorted row -> assignment t*K + k
+    float* Y;              // [T][H]: the down epilogue adds into it (accumulate != 0)
+    int Kr;                // experts per token
+    int accumulate;        // 1: atomic adds into Y; 0: fp16 rows into yp, then the combine
     uint32_t* err;
     uint32_t* st;
 };
@@ -569,6 +574,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             __half* yout = nullptr;
             if (MODE == MODE_GATEUP) hout = p.abuf + (size_t)it.row0 * p.I + it.m * 64 + (q >> 1);
             else yout = p.yp + (size_t)it.row0 * p.H + it.m * 128 + q;
+            float* yacc = p.Y + it.m * 128 + q;  // accumulate: row t of Y at + t * H
             for (int c0 = 0; c0 < n_mma && have; c0 += 32) {
                 float acc[32];
                 tmem_ld16(tq + buf * P2_BN + c0, *reinterpret_cast<float(*)[16]>(acc));
@@ -587,13 +593,26 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                             hout[(size_t)col * p.I] = __float2half_rn(silu_fast(acc[j]) * other);
                     }
                 } else {
-                    // the routing weights of these 32 columns, one per lane
-                    const float wl = c0 + lane < it.ncount ? p.wp[it.row0 + c0 + lane] : 0.f;
+                    // the routing weights (and, accumulating, the tokens) of these
+                    // 32 columns, one per lane
+                    const bool lv = c0 + lane < it.ncount;
+                    const float wl = lv ? p.wp[it.row0 + c0 + lane] : 0.f;
+                    if (p.accumulate) {
+                        const int tl = lv ? p.perm[it.row0 + c0 + lane] / p.Kr : 0;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = c0 + j;
-                        const float wj = __shfl_sync(0xffffffffu, wl, j);
-                        if (col < it.ncount) yout[(size_t)col * p.H] = __float2half_rn(wj * acc[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = c0 + j;
+                            const float wj = __shfl_sync(0xffffffffu, wl, j);
+                            const int tj = __shfl_sync(0xffffffffu, tl, j);
+                            if (col < it.ncount) atomicAdd(yacc + (size_t)tj * p.H, wj * acc[j]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = c0 + j;
+                            const float wj = __shfl_sync(0xffffffffu, wl, j);
+                            if (col < it.ncount) yout[(size_t)col * p.H] = __float2half_rn(wj * acc[j]);
+                        }
                     }
                 }
             }
@@ -1162,6 +1181,15 @@ int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, con
     gp.abuf = w.abuf;
     gp.yp = w.yp;
     gp.wp = w.wp;
+    gp.perm = w.perm;
+    gp.Y = Y;
+    gp.Kr = K;
+    // Y = sum_k w_k expert_k(x): by default the down epilogue adds each
+    // weighted row into Y with fp32 atomics (the order of a token's K terms
+    // varies from run to run); E0MOE_PREFILL_FIXED_ORDER=1 keeps fp16 rows and
+    // sums them in a fixed order (identical bits on every run)
+    const char* fo = getenv("E0MOE_PREFILL_FIXED_ORDER");
+    gp.accumulate = (fo && atoi(fo) != 0) ? 0 : 1;
     gp.err = w.err;
     gp.st = st;
 
@@ -1195,9 +1223,10 @@ int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, con
     k_umma2<MODE_GATEUP><<<num_sms(), P2_THREADS, gemm2_smem(), s>>>(mGU, mXp, gp);
     gp.K = I;
     gp.rows_out = H;
+    if (gp.accumulate && cudaMemsetAsync(Y, 0, (size_t)T * H * 4, s) != cudaSuccess) return E0_ERR_CUDA;
     k_umma2<MODE_DOWN><<<num_sms(), P2_THREADS, gemm2_smem(), s>>>(mDN, mA, gp);
-    // 7. combine
-    k_prefill_combine<<<T, 256, 0, s>>>(w.yp, w.pos, T, K, H, Y);
+    // 7. combine (fixed order only)
+    if (!gp.accumulate) k_prefill_combine<<<T, 256, 0, s>>>(w.yp, w.pos, T, K, H, Y);
     // a GEMM that gave up waiting surfaces as E0_ST_TIMEOUT
     k_err_to_status<<<1, 32, 0, s>>>(w.err, st);
     if (cudaGetLastError() != cudaSuccess) return E0_ERR_CUDA;

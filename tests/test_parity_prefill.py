@@ -57,11 +57,16 @@ def run_prefill(L, pool, X16, Wr, rp, T):
     return Y.cpu().numpy(), inds.cpu().numpy(), w.cpu().numpy(), L.e0_read_status(st)
 
 
-def test_prefill_repeated_calls_on_changing_buffers(L):
+@pytest.mark.parametrize("fixed_order", [False, True])
+def test_prefill_repeated_calls_on_changing_buffers(L, fixed_order, monkeypatch):
     """Calls that alternate two input buffers (and a larger token count in
-    between) through one workspace: each call matches the oracle, and a
-    repeated call gives the same bits (the encoded tensor maps are reused
-    only for the buffers they were made for; no state leaks between calls)."""
+    between) through one workspace: each call matches the oracle (the encoded
+    tensor maps are reused only for the buffers they were made for; no state
+    leaks between calls).  A repeated call gives the same routing and, with
+    E0MOE_PREFILL_FIXED_ORDER=1, the same bits; by default the K weighted
+    rows of a token are added with atomics, so the sum may differ in its
+    last bits from run to run."""
+    monkeypatch.setenv("E0MOE_PREFILL_FIXED_ORDER", "1" if fixed_order else "0")
     from int4_gathered_expert_gb300.model import SlotPoolDev
     d1 = synth.tiny_layer(3, T=200)
     d2 = synth.tiny_layer(4, T=200)
@@ -92,8 +97,11 @@ def test_prefill_repeated_calls_on_changing_buffers(L):
         errs = [rel_l2(Y[t], Yo[t]) for t in range(xs[i].shape[0]) if t not in ex]
         assert max(errs) <= REL_L2, max(errs)
     for a, b in ((runs[0], runs[3]), (runs[1], runs[4])):
-        for u, v in zip(a, b):
-            assert np.array_equal(u, v)
+        assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+        if fixed_order:
+            assert np.array_equal(a[0], b[0])
+        else:
+            assert np.abs(a[0] - b[0]).max() <= 1e-6 * np.abs(a[0]).max()
 
 
 @pytest.mark.parametrize("T", [1, 8, 130, 513])
