@@ -44,7 +44,7 @@ struct PrefillWs {
     int32_t* pos;       // [T*K]  assignment -> sorted position
     int32_t* seg_cnt;   // [nseg][E]
     int32_t* seg_base;  // [nseg][E]
-    int4* tiles;        // [max_tiles] {expert, first sorted row, n0, rows}
+    int4* tiles;        // [max_tiles] {expert, first sorted row, n0, rows}, most rows first
     int32_t* flag;      // [T+1] tokens whose routing is recomputed in fp32 (count first)
     int32_t* n_tiles;   // [1]
     uint32_t* err;      // [1] timeouts inside the GEMMs
@@ -370,6 +370,15 @@ struct P2Item {
     int slot, row0, ncount, m;
 };
 
+// The item a CTA takes in round k: round-robin over the CTAs, in alternating
+// directions, so that the heaviest items (first in the tile order) spread
+// evenly.  Later rounds hold larger positions, so a CTA stops at the first
+// position past the last item.
+E0_DEV int p2_pos(int k) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return k * G + ((k & 1) ? G - 1 - c : c);
+}
+
 E0_DEV P2Item p2_item(const GemmP& p, int idx, int MT) {
     const int4 tl = p.tiles[idx / MT];
     P2Item it;
@@ -473,7 +482,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         const int r = q4 * 32 + lane;
         uint32_t gbase = 0;  // global step of the item's first K step
         bool ok = true;
-        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        for (int k = 0, idx; (idx = p2_pos(k)) < n_items && ok; ++k) {
             const P2Item it = p2_item(p, idx, MT);
             const uint8_t* ex = it.slot >= 0 ? p.pool + (size_t)it.slot * p.slot_bytes : nullptr;
             const int wr = it.m * 128 + r;  // weight row (interleaved gate/up rows for MODE_GATEUP)
@@ -558,7 +567,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         const int q = threadIdx.x - 128;  // TMEM lane
         const uint32_t tq = tmem + ((uint32_t)((warp - 4) * 32) << 16);
         uint32_t ii = 0;
-        for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++ii) {
+        for (int k = 0, idx; (idx = p2_pos(k)) < n_items; ++k, ++ii) {
             const P2Item it = p2_item(p, idx, MT);
             const uint32_t buf = ii & 1;
             const bool have = mbar_wait(&acc_full[buf], (ii >> 1) & 1, abort, WAIT_LIMIT_NS);
@@ -626,7 +635,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             tma_prefetch_desc(&tmCodes);
             uint32_t g = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            for (int k = 0, idx; (idx = p2_pos(k)) < n_items && ok; ++k) {
                 const P2Item it = p2_item(p, idx, MT);
                 const int z = it.slot >= 0 ? it.slot : 0;
                 for (int kk = 0; kk < nk; ++kk, ++g) {
@@ -655,7 +664,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             tma_prefetch_desc(&tmB);
             uint32_t g = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            for (int k = 0, idx; (idx = p2_pos(k)) < n_items && ok; ++k) {
                 const P2Item it = p2_item(p, idx, MT);
                 for (int kk = 0; kk < nk; ++kk, ++g) {
                     const uint32_t os = g % P2_OP_STAGES;
@@ -680,7 +689,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         if (lane == 0) {
             uint32_t g = 0, ii = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++ii) {
+            for (int k = 0, idx; (idx = p2_pos(k)) < n_items && ok; ++k, ++ii) {
                 const P2Item it = p2_item(p, idx, MT);
                 const uint32_t buf = ii & 1;
                 if (!mbar_wait(&acc_empty[buf], ((ii >> 1) + 1) & 1, abort, WAIT_LIMIT_NS)) {
@@ -954,12 +963,20 @@ __global__ void k_prefill_reroute(const float* logits, int E, RouteP rp, const i
 // tiles of up to BN consecutive sorted rows of one expert: {e, first row, n0, rows}
 __global__ void k_prefill_tiles(const int32_t* counts, const int32_t* offsets, int E, int4* tiles,
                                 int32_t* n_tiles) {
+    // tiles of up to BN consecutive sorted rows of one expert, heaviest
+    // first: every full tile (BN rows) in expert order, then each expert's
+    // partial tile by rows, most first (ties to the lower expert).  The
+    // grouped GEMMs hand their items out in this order, in alternating
+    // directions, so that the CTAs get similar loads.
     __shared__ int32_t warp_tot[32];
+    __shared__ int32_t part_rows[1024];
     const int e = threadIdx.x;
     const int c = e < E ? counts[e] : 0;
-    const int nt = (c + BN - 1) / BN;
+    const int nfull = c / BN, rem = c % BN;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = nt;
+    part_rows[e] = rem;
+    // exclusive scan of the full tiles over the experts
+    int incl = nfull;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int t = __shfl_up_sync(0xffffffffu, incl, o);
@@ -977,12 +994,22 @@ __global__ void k_prefill_tiles(const int32_t* counts, const int32_t* offsets, i
         warp_tot[lane] = v;
     }
     __syncthreads();
-    const int start = incl - nt + (warp > 0 ? warp_tot[warp - 1] : 0);
-    for (int j = 0; j < nt; ++j) {
-        const int n0 = j * BN;
-        tiles[start + j] = make_int4(e, offsets[e] + n0, n0, min(BN, c - n0));
+    const int start = incl - nfull + (warp > 0 ? warp_tot[warp - 1] : 0);
+    const int n_full = warp_tot[(blockDim.x - 1) >> 5];
+    for (int j = 0; j < nfull; ++j) tiles[start + j] = make_int4(e, offsets[e] + j * BN, j * BN, BN);
+    if (rem > 0) {
+        int rank = 0;
+        for (int f = 0; f < E; ++f) {
+            const int rf = part_rows[f];
+            rank += rf > rem || (rf == rem && f < e);
+        }
+        tiles[n_full + rank] = make_int4(e, offsets[e] + nfull * BN, nfull * BN, rem);
     }
-    if (threadIdx.x == blockDim.x - 1) *n_tiles = incl + (warp > 0 ? warp_tot[warp - 1] : 0);
+    if (threadIdx.x == 0) {
+        int n_part = 0;
+        for (int f = 0; f < E; ++f) n_part += part_rows[f] > 0;
+        *n_tiles = n_full + n_part;
+    }
 }
 
 // xp[p] = X[token of perm[p]], wp[p] = w[perm[p]]
