@@ -203,10 +203,13 @@ class StreamedStack:
 
     The decode launches leave ``free_sms`` SMs to the copy kernels, which run
     on that many blocks: a cooperative launch over every SM would wait for a
-    running copy kernel instead of overlapping it."""
+    running copy kernel instead of overlapping it.  The layers of one half
+    are prefetched with one batched call (``batched=False``: one call per
+    layer, the same slot contents)."""
 
     def __init__(self, sd: "StackDev", split: int, device="cuda", cache: Optional["ExpertCacheDev"] = None,
-                 host: Optional[dict] = None, free_sms: int = 24):
+                 host: Optional[dict] = None, free_sms: int = 24, batched: bool = True):
+        self.batched = batched
         import os
         old = os.environ.get("E0MOE_LL_FREE_SMS")
         os.environ["E0MOE_LL_FREE_SMS"] = str(int(free_sms))
@@ -248,6 +251,15 @@ class StreamedStack:
         return L.e0_slot_bytes(self.sd.H, self.sd.I)
 
     def _prefetch(self, layers, t_next, stream):
+        if not self.batched:
+            for l in layers:
+                if self.cache is None:
+                    L.e0_stack_prefetch_experts(self.sd.ws, l, t_next, self.pools[l].desc, self.host[l], self.status,
+                                                stream=stream)
+                else:
+                    L.e0_stack_prefetch_experts_cached(self.sd.ws, l, t_next, self.pools[l].desc, self.host[l],
+                                                       self.cache.desc, self.status, stream=stream)
+            return
         # every layer of the batch in one copy launch and one commit launch
         pools = [self.pools[l].desc for l in layers]
         banks = [self.host[l] for l in layers]

@@ -297,6 +297,33 @@ def test_streamed_stack_matches_oracle(L, overlap):
         assert 0 < (tab >= 0).sum() <= 2 * m.shape.layer.K
 
 
+@pytest.mark.parametrize("capacity", [0, 3])
+def test_streamed_stack_per_layer_prefetch_equals_batched(L, capacity):
+    """The per-layer prefetch calls (plain, and through a small cache that
+    evicts) fill the slots exactly as the batched calls do: the decode of
+    every token gives the same bits."""
+    from int4_gathered_expert_gb300.model import ExpertCacheDev, StackDev, StreamedStack
+    m = _tiny_stream_model()
+    X = torch.from_numpy(m.x).cuda()
+    runs = []
+    for batched in (True, False):
+        sd = StackDev(m, trace=True)
+        cache = ExpertCacheDev(capacity, sd.L, sd.H, sd.I, sd.E) if capacity else None
+        ss = StreamedStack(sd, split=5, cache=cache, batched=batched)
+        ss.start(X[0])
+        got = [snapshot(sd)]
+        for t in range(1, 6):
+            ss.step(X[t])
+            torch.cuda.synchronize()
+            got.append(snapshot(sd))
+        assert L.e0_read_status(sd.status) == 0
+        runs.append(got)
+        del ss, sd, cache
+    for t in range(6):
+        for k in ("r", "inds", "w", "pred_inds"):
+            assert np.array_equal(runs[0][t][k], runs[1][t][k]), (t, k)
+
+
 @pytest.mark.parametrize("capacity", [3, 64])
 def test_streamed_stack_with_expert_cache(L, capacity):
     """Staged streaming with a cross-layer LRU cache of expert bundles in front
