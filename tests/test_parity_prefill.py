@@ -57,6 +57,29 @@ def run_prefill(L, pool, X16, Wr, rp, T):
     return Y.cpu().numpy(), inds.cpu().numpy(), w.cpu().numpy(), L.e0_read_status(st)
 
 
+def test_prefill_many_experts(L):
+    """E = 1024 (the largest E the library takes) at the tiny layer width,
+    K = 2, T = 700: nearly every expert gets a partial tile, so the tile list
+    ranks ~1000 partial tiles, and every token's routing and output is
+    checked against the oracle."""
+    import dataclasses
+    from int4_gathered_expert_gb300.model import SlotPoolDev
+    s = dataclasses.replace(synth.TINY, E=1024, K=2)
+    T = 700
+    bank = synth.expert_bank(11, 0, s)
+    W_r = synth.router(11, 0, s)
+    X = synth.normal_rows(11, T, s.H).astype(np.float16)
+    pool = SlotPoolDev.resident(bank, s.H, s.I)
+    Y, inds, w, st = run_prefill(L, pool, dev(X), dev(W_r), L.route_params(K=s.K), T)
+    assert st == 0
+    Yo, rt = O.prefill(X, bank, W_r, s)
+    ex, msgs = routing_matches(inds, w, rt)
+    assert not msgs, msgs[:4]
+    assert len(np.unique(inds)) > 600
+    errs = [rel_l2(Y[t], Yo[t]) for t in range(T) if t not in ex]
+    assert max(errs) <= REL_L2, max(errs)
+
+
 @pytest.mark.parametrize("fixed_order", [False, True])
 def test_prefill_repeated_calls_on_changing_buffers(L, fixed_order, monkeypatch):
     """Calls that alternate two input buffers (and a larger token count in
