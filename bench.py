@@ -13,7 +13,8 @@ iterations.
 
 The same JSON line also carries: the end-to-end rate through the C ABI with
 host buffers (e2e), the CPU oracle on all host cores (cpu_baseline) and on one
-thread for the single-layer workloads (cpu_oracle_one_thread), the K x
+thread for the single-layer workloads and the 8B and 35B stacks
+(cpu_oracle_one_thread, run in a child process beside the GPU work), the K x
 prerouter on/off sweep on the same weights (route_sweep), the 35B-tier single
 layer alone at T=1 and T=8 (block_35b), the 8B-tier 24-layer stack
 (stack_8b), the host-tier staged streaming run (streaming: consumer layers'
@@ -147,7 +148,10 @@ def run_prefill_bench(dev, reps: int = 5, tier: str = "35b"):
                          "traffic": recorded_traffic("k_umma2<1>") if tier == "35b" else None,
                          "traffic_kernel": "k_umma2<1>" if tier == "35b" else None,
                          "peak_source": "MEASURED_PEAKS.json bf16_tflops (measured, fp16 = bf16 rate)"
-                         if pk else "fallback"},
+                         if pk else "fallback",
+                         # the same rate against the GEMM rate held for seconds under the power cap
+                         "peak_sustained": pk.get("bf16_tflops_sustained") if pk else 1700.0,
+                         "frac_sustained": flops / t / 1e12 / (pk.get("bf16_tflops_sustained") if pk else 1700.0)},
             "l2": "flushed (256 MB write) before each timed call",
             "timing": "device time, calls enqueued ahead of the GPU; ms_idle_start: the same call started on an "
                       "idle GPU (host encoding and launches inside the timed region)",
@@ -309,7 +313,9 @@ def run_stack8b_bench(dev, n_warm: int = 8, n_timed: int = 128):
             "value": 1.0 / s_tok, "unit": "tok/s", "us_per_token": s_tok * 1e6, "tokens": n_timed,
             "bytes_per_token": nb, "weight_gbs": nb["total"] / s_tok / 1e9,
             "roofline": {"bound": "hbm", "achieved": nb["total"] / s_tok / 1e9, "peak": peak, "unit": "GB/s",
-                         "frac": nb["total"] / s_tok / 1e9 / peak, "kernel": "k_stack_ll"},
+                         "frac": nb["total"] / s_tok / 1e9 / peak, "kernel": "k_stack_ll",
+                         "peak_nominal": HBM_NOMINAL_GBS,
+                         "frac_nominal": nb["total"] / s_tok / 1e9 / HBM_NOMINAL_GBS},
             "device_status": st}
 
 
@@ -337,7 +343,7 @@ def run_route_sweep(sd, X, n_warm: int = 8, n_timed: int = 96):
 
 
 ORACLE_ONE_THREAD = r"""
-import json, sys, time
+import gc, json, sys, time
 import numpy as np
 sys.path.insert(0, sys.argv[1])
 from oracle import e0_oracle as O
@@ -356,22 +362,49 @@ res["tiny_T8_ms"] = 1e3 * min(blk(d, 8) for _ in range(3))
 d = synth.layer35b(1, T=8)
 for T in (1, 8):
     res["l35b_T%d_ms" % T] = 1e3 * blk(d, T)
+del d
+for name, shape in (("stack_8b", synth.STACK8B), ("stack_35b", synth.STACK35B)):
+    m = synth.stack_model(shape, n_tokens=2)
+    st = O.StackState(shape.n_layers)
+    t = []
+    for i in range(2):
+        t0 = time.perf_counter()
+        O.stack_token(m.x[i], m, st)
+        t.append(time.perf_counter() - t0)
+    res[name] = {"token0_s": t[0], "steady_token_s": t[1], "tok_s": 1.0 / t[1],
+                 "tokens_8_s_extrapolated": t[0] + 7 * t[1]}
+    del m, st
+    gc.collect()
 print(json.dumps(res))
 """
 
 
-def time_oracle_one_thread():
-    """The oracle's MoE block (routing + experts) on one host thread: the tiny
-    layer (T=8) and the 35B-tier single layer (T=1, T=8)."""
+def start_oracle_one_thread():
+    """Starts, in a child process with BLAS limited to one thread, the
+    oracle's MoE block (routing + experts) on the tiny layer (T=8) and the
+    35B-tier single layer (T=1, T=8), then the 8B and 35B stacks for two
+    tokens each: token 0 (every layer routes natively) and one steady-state
+    token.  Eight tokens are extrapolated as token 0 + 7 steady tokens.  The
+    child runs on one host core while the GPU measurements go on."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    return subprocess.Popen([sys.executable, "-c", ORACLE_ONE_THREAD, ROOT], env=env, stdout=subprocess.PIPE,
+                            stderr=subprocess.PIPE, text=True)
+
+
+def finish_oracle_one_thread(proc, timeout: float = 600.0):
     try:
-        p = subprocess.run([sys.executable, "-c", ORACLE_ONE_THREAD, ROOT], env=env, capture_output=True, text=True,
-                           timeout=600)
-        r = json.loads(p.stdout.strip().splitlines()[-1])
-    except (subprocess.SubprocessError, ValueError, IndexError) as ex:
+        out, _ = proc.communicate(timeout=timeout)
+        r = json.loads(out.strip().splitlines()[-1])
+    except subprocess.TimeoutExpired as ex:
+        proc.kill()
+        proc.communicate()
+        return {"error": repr(ex)[:200]}
+    except (ValueError, IndexError) as ex:
         return {"error": repr(ex)[:200]}
     r.update({"cores": 1, "kind": "oracle",
-              "sample": "one call of the float64 numpy oracle's routing + MoE block, BLAS limited to one thread"})
+              "sample": "float64 numpy oracle, BLAS limited to one thread: one call of the routing + MoE block "
+                        "(tiny layer, 35B-tier layer); the 8B and 35B stacks for token 0 and one steady token, "
+                        "tokens_8_s_extrapolated = token 0 + 7 x the steady token (extrapolated, not measured)"})
     return r
 
 
@@ -632,6 +665,9 @@ def whole_job_rate(units_per_rank: int, world: int, seconds_max: float) -> float
     return world * units_per_rank / seconds_max
 
 
+# GB300 HBM3e bandwidth as specified (the measured copy rate is the roofline's peak)
+HBM_NOMINAL_GBS = 8000.0
+
 # launches of this library's kernels per decode token, by stack implementation
 LAUNCHES_PER_TOKEN = {0: 1, 3: 1}
 KERNEL_NAME = {0: "k_stack_token", 1: "k_stack_gateup/k_stack_down chain", 3: "k_stack_ll"}
@@ -825,6 +861,9 @@ def run_gb300(args):
         sd = None
 
     block = stack8b = oracle1 = None
+    oracle1_proc = None
+    if rank == 0 and ws == 1 and not args.no_extras and not args.no_cpu:
+        oracle1_proc = start_oracle_one_thread()
     if rank == 0 and not args.no_extras:
         del sd
         sd = None
@@ -833,8 +872,6 @@ def run_gb300(args):
         torch.cuda.empty_cache()
         stack8b = run_stack8b_bench(dev)
         torch.cuda.empty_cache()
-        if ws == 1 and not args.no_cpu:
-            oracle1 = time_oracle_one_thread()
 
     prefill = prefill8 = None
     if rank == 0 and not args.no_prefill:
@@ -844,6 +881,8 @@ def run_gb300(args):
         prefill = run_prefill_bench(dev)
         torch.cuda.empty_cache()
         prefill8 = run_prefill_bench(dev, tier="8b")
+    if oracle1_proc is not None:
+        oracle1 = finish_oracle_one_thread(oracle1_proc)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
@@ -866,7 +905,8 @@ def run_gb300(args):
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "traffic": traffic,
                              "kernel": kname, "launch_us": mean_launch_s * 1e6,
-                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback"},
+                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback",
+                             "peak_nominal": HBM_NOMINAL_GBS, "frac_nominal": achieved / HBM_NOMINAL_GBS},
                 "cpu_baseline": cpu, "cpu_oracle_one_thread": oracle1, "e2e": e2e, "prefill": prefill,
                 "prefill_8b": prefill8, "stack_8b": stack8b, "block_35b": block, "route_sweep": sweep,
                 "streaming": streaming,
