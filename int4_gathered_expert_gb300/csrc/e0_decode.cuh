@@ -78,9 +78,15 @@ E0_DEV float float_of_order_key(uint32_t k) {
 // One warp routes one token.  Ranking uses the fp32 logits (softmax and
 // sigmoid are monotonic), ties go to the lower expert id, output is in
 // descending score order.  scr: E floats of per-warp shared scratch.
-template <int MAXM>
-E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds, float* w, float* scr,
-                         uint32_t* st, int lane) {
+// With GAP the selection runs one round further and the function returns
+// (the same in every lane) the smallest distance between consecutive ranked
+// scores among the K + 1 largest (biased) logits, and, in group-limited
+// routing, between the G-th and (G+1)-th group scores: a routing that a
+// smaller logit error could change has a gap below that error.  Without GAP
+// it returns +inf.
+template <int MAXM, bool GAP = false>
+E0_DEV float route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds, float* w, float* scr,
+                          uint32_t* st, int lane) {
     // scores are held as order keys (see float_order_key): ranking needs
     // only their order, and the winners' values are decoded from the keys
     uint32_t key[MAXM];
@@ -103,6 +109,7 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
 #pragma unroll
     for (int m = 0; m < MAXM; ++m)
         if (lane + 32 * m < E) alive |= 1u << m;
+    float gap = INFINITY;
 
     if (rp.mode == E0_ROUTE_SIGMOID_GROUP) {
         const int n = rp.n_groups, gsz = E / rp.n_groups;
@@ -128,8 +135,10 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
         }
         __syncwarp();
         uint32_t kept = 0;
-        float gv = gscore;
-        for (int r = 0; r < rp.topk_groups; ++r) {
+        float gv = gscore, gprev = 0.f;
+        // with GAP, one more round finds the best group left out
+        const int g_rounds = GAP ? min(rp.topk_groups + 1, n) : rp.topk_groups;
+        for (int r = 0; r < g_rounds; ++r) {
             float bv = gv;
             int bi = lane < n ? lane : 64 + lane;
             if (lane < n && (kept >> lane & 1u)) {
@@ -145,6 +154,11 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
                     bi = oi;
                 }
             }
+            if (GAP && r == rp.topk_groups) {
+                if (bi < n) gap = fminf(gap, gprev - bv);
+                break;
+            }
+            gprev = bv;
             if (bi < n) kept |= 1u << bi;
         }
 #pragma unroll
@@ -158,8 +172,8 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
     // largest order key (a float's order as an unsigned integer, 0 for "no
     // candidate"), then the lowest expert id holding it.
     int my_ind = -1;
-    float my_val = 0.f;
-    for (int k = 0; k < rp.K; ++k) {
+    float my_val = 0.f, eprev = 0.f;
+    for (int k = 0; k < (GAP ? rp.K + 1 : rp.K); ++k) {
         uint32_t bk = 0;
         uint32_t bi = 0xffffffffu;
 #pragma unroll
@@ -172,6 +186,12 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
         if (mk == 0) break;  // fewer candidates than K (validated away on the host)
         const uint32_t wi = __reduce_min_sync(0xffffffffu, bk == mk ? bi : 0xffffffffu);
         if ((int)(wi & 31) == lane) alive &= ~(1u << (wi >> 5));
+        if (GAP) {
+            const float v = float_of_order_key(mk);
+            if (k > 0) gap = fminf(gap, eprev - v);
+            eprev = v;
+            if (k == rp.K) break;
+        }
         if (lane == k) {
             my_ind = (int)wi;
             my_val = float_of_order_key(mk);
@@ -192,6 +212,7 @@ E0_DEV void route_warp_t(const float* lg, int E, const RouteP& rp, int32_t* inds
         inds[lane] = my_ind;
         w[lane] = wk;
     }
+    return gap;
 }
 
 static __device__ __noinline__ void route_warp(const float* lg, int E, const RouteP& rp, int32_t* inds, float* w, float* scr, uint32_t* st,

@@ -744,177 +744,48 @@ static size_t gemm2_smem() {
 
 // ------------------------------------------------------------------ small prefill kernels
 
-// Smallest gap between consecutive scores among the K+1 largest of one
-// token's (biased) logits, one warp: K+1 rounds of two warp reductions over
-// order keys (the same ranking as the routing itself).
+// Route one token per warp from the tensor-core logits and flag the tokens
+// whose routing a logit error below REFINE_GAP could change: the selection
+// runs one round past K (and, in group-limited routing, one past G groups)
+// and a token is flagged where two consecutive scores of the K + 1 largest,
+// or the G-th and (G+1)-th group scores, are closer than that.  A group score
+// (the sum of a group's two largest sigmoids) moves by at most half the logit
+// error (sigmoid' <= 1/4, two terms), so one threshold serves both gaps.
+// MAXM = ceil(E / 32) keys a lane.
 template <int MAXM>
-__device__ float topk_gap_t(const float* lg, int E, const float* bias, int K, int lane) {
-    uint32_t key[MAXM];
-    uint32_t alive = 0;
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m) {
-        const int e = lane + 32 * m;
-        key[m] = 0;
-        if (e < E) {
-            float x = __ldcg(lg + e) + (bias ? bias[e] : 0.f);
-            if (!isfinite(x)) x = -INFINITY;
-            key[m] = float_order_key(x);
-            alive |= 1u << m;
-        }
-    }
-    float prev = 0.f, mingap = INFINITY;
-    for (int k = 0; k <= K && k < E; ++k) {
-        uint32_t bk = 0, bi = 0xffffffffu;
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m)
-            if (((alive >> m) & 1u) && key[m] > bk) {
-                bk = key[m];
-                bi = (uint32_t)(lane + 32 * m);
-            }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-        if (mk == 0) break;
-        const uint32_t wi = __reduce_min_sync(0xffffffffu, bk == mk ? bi : 0xffffffffu);
-        if ((int)(wi & 31) == lane) alive &= ~(1u << (wi >> 5));
-        const float v = float_of_order_key(mk);
-        if (k > 0) mingap = fminf(mingap, prev - v);
-        prev = v;
-    }
-    return mingap;
-}
-
-__device__ float topk_gap(const float* lg, int E, const float* bias, int K, int lane) {
-    if (E <= 32) return topk_gap_t<1>(lg, E, bias, K, lane);
-    if (E <= 64) return topk_gap_t<2>(lg, E, bias, K, lane);
-    if (E <= 128) return topk_gap_t<4>(lg, E, bias, K, lane);
-    if (E <= 256) return topk_gap_t<8>(lg, E, bias, K, lane);
-    if (E <= 512) return topk_gap_t<16>(lg, E, bias, K, lane);
-    return topk_gap_t<32>(lg, E, bias, K, lane);
-}
-
-// Sigmoid group-limited routing: a decision can change under a small logit
-// error only where the G-th and (G+1)-th group scores (sum of a group's two
-// largest sigmoids) are close, or where the K-th and (K+1)-th logits among
-// the experts of the kept groups are (the sigmoid is monotone).  A group
-// score moves by at most half the logit error (sigmoid' <= 1/4, two terms),
-// so one threshold serves both gaps.  One warp per token.
-template <int MAXM>
-__device__ bool sg_near_tie_t(const float* lg, int E, int n, int G, int K, float gap, int lane) {
-    const int per = E / n;
-    uint32_t key[MAXM];
-    float sg[MAXM];
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m) {
-        const int e = lane + 32 * m;
-        key[m] = 0;
-        sg[m] = -INFINITY;
-        if (e < E) {
-            float x = __ldcg(lg + e);
-            if (!isfinite(x)) x = -INFINITY;
-            key[m] = float_order_key(x);
-            sg[m] = 1.f / (1.f + __expf(-x));
-        }
-    }
-    // group scores: lane g (< n) keeps the score of group g
-    float my_gs = -INFINITY;
-    for (int g = 0; g < n; ++g) {
-        float a = -INFINITY, b = -INFINITY;  // this lane's two largest sigmoids of group g
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-            const int e = lane + 32 * m;
-            if (e < E && e / per == g) {
-                if (sg[m] > a) {
-                    b = a;
-                    a = sg[m];
-                } else if (sg[m] > b) {
-                    b = sg[m];
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float a2 = __shfl_xor_sync(0xffffffffu, a, o), b2 = __shfl_xor_sync(0xffffffffu, b, o);
-            const float hi = fmaxf(a, a2), lo = fmaxf(fminf(a, a2), fmaxf(b, b2));
-            a = hi;
-            b = lo;
-        }
-        if (lane == g) my_gs = a + b;
-    }
-    // G-th vs (G+1)-th group score; the kept groups (ties to the lower index)
-    uint32_t gkey = lane < n ? float_order_key(my_gs) : 0u;
-    uint32_t kept = 0;
-    float prev = 0.f, ggap = INFINITY;
-    for (int k = 0; k <= G && k < n; ++k) {
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, gkey);
-        const uint32_t wi = __reduce_min_sync(0xffffffffu, (gkey == mk && lane < n) ? (uint32_t)lane : 0xffffffffu);
-        if (wi >= 32u) break;
-        const float v = float_of_order_key(mk);
-        if (k == G) ggap = prev - v;  // only the boundary between kept and dropped groups matters
-        prev = v;
-        if (k < G) kept |= 1u << wi;
-        if ((uint32_t)lane == wi) gkey = 0;
-    }
-    if (G < n && ggap < gap) return true;
-    // K-th vs (K+1)-th logit among the kept groups' experts
-    uint32_t alive = 0;
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m) {
-        const int e = lane + 32 * m;
-        if (e < E && ((kept >> (e / per)) & 1u)) alive |= 1u << m;
-    }
-    float eprev = 0.f, egap = INFINITY;
-    for (int k = 0; k <= K; ++k) {
-        uint32_t bk = 0, bi = 0xffffffffu;
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m)
-            if (((alive >> m) & 1u) && key[m] > bk) {
-                bk = key[m];
-                bi = (uint32_t)(lane + 32 * m);
-            }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-        if (mk == 0) break;
-        const uint32_t wi = __reduce_min_sync(0xffffffffu, bk == mk ? bi : 0xffffffffu);
-        if ((int)(wi & 31) == lane) alive &= ~(1u << (wi >> 5));
-        const float v = float_of_order_key(mk);
-        if (k > 0) egap = fminf(egap, eprev - v);
-        eprev = v;
-    }
-    return egap < gap;
-}
-
-__device__ bool sg_near_tie(const float* lg, int E, const RouteP& rp, float gap, int lane) {
-    if (rp.n_groups < 1 || rp.n_groups > 32 || E % rp.n_groups) return true;  // not expected: refine
-    if (E <= 32) return sg_near_tie_t<1>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
-    if (E <= 64) return sg_near_tie_t<2>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
-    if (E <= 128) return sg_near_tie_t<4>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
-    if (E <= 256) return sg_near_tie_t<8>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
-    if (E <= 512) return sg_near_tie_t<16>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
-    return sg_near_tie_t<32>(lg, E, rp.n_groups, rp.topk_groups, rp.K, gap, lane);
-}
-
-// Route one token per warp from the tensor-core logits; flag tokens whose
-// routing a logit error below REFINE_GAP could change.
-__global__ void k_prefill_route(const float* logits, int T, int E, RouteP rp, int32_t* inds, float* w,
-                                int32_t* flag, uint32_t* st) {
+__global__ void __launch_bounds__(256) k_prefill_route(const float* logits, int T, int E, RouteP rp, int32_t* inds,
+                                                       float* w, int32_t* flag, uint32_t* st) {
     extern __shared__ float scr[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
     if (t >= T) return;
-    const float* lg = logits + (size_t)t * E;
-    route_warp(lg, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr + warp * E, st, lane);
-    // softmax routing is refined where two of the K+1 largest scores are close,
-    // sigmoid-group routing where a group or an expert decision is
-    const bool refine = rp.mode == E0_ROUTE_SOFTMAX_TOPK ? topk_gap(lg, E, rp.logit_bias, rp.K, lane) < REFINE_GAP
-                                                         : sg_near_tie(lg, E, rp, REFINE_GAP, lane);
-    if (lane == 0 && refine) flag[1 + atomicAdd(flag, 1)] = t;
+    const float gap = route_warp_t<MAXM, true>(logits + (size_t)t * E, E, rp, inds + (size_t)t * rp.K,
+                                               w + (size_t)t * rp.K, scr + warp * E, st, lane);
+    // a group count the ranking does not expect is always refined
+    const bool odd = rp.mode == E0_ROUTE_SIGMOID_GROUP && (rp.n_groups < 1 || rp.n_groups > 32 || E % rp.n_groups);
+    if (lane == 0 && (odd || !(gap >= REFINE_GAP))) flag[1 + atomicAdd(flag, 1)] = t;
 }
 
 // fp16 row slice (64 halves) . fp16 x slice (64 halves), fp32 accumulation
+// Read-only 16-byte load kept in source order (volatile), so that all of a
+// lane's loads are issued before the first product: one memory round trip.
+E0_DEV uint4 ldg_nc_ordered(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
 E0_DEV float hh64_dot(const __half* wrow, const __half* x) {
+    uint4 wq[8], xq[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        wq[c] = ldg_nc_ordered(wrow + 8 * c);
+        xq[c] = ldg_nc_ordered(x + 8 * c);
+    }
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        const uint4 wv = ldg_stream(wrow + 8 * c);
-        const uint4 xv = *reinterpret_cast<const uint4*>(x + 8 * c);
+        const uint4 wv = wq[c];
+        const uint4 xv = xq[c];
         const __half2* xh = reinterpret_cast<const __half2*>(&xv);
         float xs[8];
 #pragma unroll
@@ -947,17 +818,41 @@ __global__ void __launch_bounds__(256) k_prefill_refine_logits(const __half* X, 
 }
 
 // Route the flagged tokens again from their exact logits (one warp each).
-__global__ void k_prefill_reroute(const float* logits, int E, RouteP rp, const int32_t* flag, int32_t* inds, float* w,
-                                  uint32_t* st) {
+template <int MAXM>
+__global__ void __launch_bounds__(256) k_prefill_reroute(const float* logits, int E, RouteP rp, const int32_t* flag,
+                                                         int32_t* inds, float* w, uint32_t* st) {
     extern __shared__ float scr[];
     const int n = flag[0];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = blockIdx.x * (blockDim.x >> 5) + warp; i < n; i += gridDim.x * (blockDim.x >> 5)) {
         const int t = flag[1 + i];
-        route_warp(logits + (size_t)t * E, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K, scr + warp * E, st,
-                   lane);
+        route_warp_t<MAXM>(logits + (size_t)t * E, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K,
+                           scr + warp * E, st, lane);
         __syncwarp();
     }
+}
+
+// Both routing kernels, instantiated for the keys a lane holds (E / 32
+// rounded up to a power of two), so that no instance carries the registers
+// of a larger E.
+static void launch_route(bool again, const float* logits, int T, int E, const RouteP& rp, const int32_t* flag_in,
+                         int32_t* flag, int32_t* inds, float* w, uint32_t* st, cudaStream_t s) {
+    const size_t sm = (size_t)8 * E * 4;
+    const unsigned grid = again ? (unsigned)num_sms() : (unsigned)((T + 7) / 8);
+#define E0_ROUTE_LAUNCH(M)                                                                    \
+    do {                                                                                      \
+        if (again)                                                                            \
+            k_prefill_reroute<M><<<grid, 256, sm, s>>>(logits, E, rp, flag_in, inds, w, st);  \
+        else                                                                                  \
+            k_prefill_route<M><<<grid, 256, sm, s>>>(logits, T, E, rp, inds, w, flag, st);    \
+    } while (0)
+    if (E <= 32) E0_ROUTE_LAUNCH(1);
+    else if (E <= 64) E0_ROUTE_LAUNCH(2);
+    else if (E <= 128) E0_ROUTE_LAUNCH(4);
+    else if (E <= 256) E0_ROUTE_LAUNCH(8);
+    else if (E <= 512) E0_ROUTE_LAUNCH(16);
+    else E0_ROUTE_LAUNCH(32);
+#undef E0_ROUTE_LAUNCH
 }
 
 // tiles of up to BN consecutive sorted rows of one expert: {e, first row, n0, rows}
@@ -1228,9 +1123,9 @@ int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, con
     // 2. routing (+ refinement of near-ties)
     int32_t* flag = w.flag;
     if (cudaMemsetAsync(flag, 0, 4, s) != cudaSuccess) return E0_ERR_CUDA;
-    k_prefill_route<<<(T + 7) / 8, 256, (size_t)8 * E * 4, s>>>(w.logits, T, E, rp, inds, wts, flag, st);
+    launch_route(false, w.logits, T, E, rp, nullptr, flag, inds, wts, st, s);
     k_prefill_refine_logits<<<num_sms() * 4, 256, 0, s>>>(X, H, W_r, E, flag, w.logits);
-    k_prefill_reroute<<<num_sms(), 256, (size_t)8 * E * 4, s>>>(w.logits, E, rp, flag, inds, wts, st);
+    launch_route(true, w.logits, T, E, rp, flag, nullptr, inds, wts, st, s);
     if (cudaGetLastError() != cudaSuccess) return E0_ERR_CUDA;
     // 3. sort
     int rc = sort_into(inds, T, K, E, w.counts, w.offsets, w.perm, w.pos, w, s);

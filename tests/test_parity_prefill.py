@@ -165,6 +165,56 @@ def test_prefill_one_crowded_expert_set(L):
     assert max(rel_l2(Y[t], Yo[t]) for t in range(T)) <= REL_L2
 
 
+@pytest.mark.parametrize("mode", ["softmax_topk", "sigmoid_group"])
+def test_prefill_planted_near_ties(L, mode):
+    """Two router rows that differ in one fp16 ulp of one input: in every token
+    their two logits differ by ulp * x_j, a few 1e-6 to 1e-5 at the 35B width,
+    the size of the tensor-core logits' own error, so their order rests on the
+    exact recomputation of the tokens flagged as near-ties.  Softmax top-k: a
+    logit bias lifts both into every token's top K; sigmoid group-limited: the
+    two share a group.  Every token whose gap is above the tie rule must route
+    as the oracle does, and many such tokens must exist."""
+    import dataclasses
+    from int4_gathered_expert_gb300.model import SlotPoolDev
+    if mode == "softmax_topk":
+        s = dataclasses.replace(synth.TINY, H=2048, E=64, K=4)
+    else:
+        s = dataclasses.replace(synth.TINY, H=2048, E=64, K=8, route="sigmoid_group", n_groups=8, topk_groups=4,
+                                route_scale=2.5)
+    T = 600
+    e0, e1 = 3, 5  # the same group of 8 experts in the sigmoid-group case
+    W = synth.router(13, 0, s, std=1.0 / np.sqrt(s.H))
+    j = int(np.argmin(np.abs(np.abs(W[e0].astype(np.float32)) - 0.02)))  # fp16 ulp 1.5e-5 there
+    W[e1] = W[e0]
+    W[e1, j] = np.nextafter(W[e0, j], np.float16(np.inf) if W[e0, j] > 0 else np.float16(-np.inf))
+    X = synth.normal_rows(13, T, s.H).astype(np.float16)
+    bank = synth.expert_bank(13, 0, s)
+    pool = SlotPoolDev.resident(bank, s.H, s.I)
+    bias = None
+    if mode == "softmax_topk":
+        bias = np.zeros(s.E, np.float32)
+        bias[[e0, e1]] = 4.0
+        bias_d = dev(bias)  # the descriptor holds a raw pointer: keep the tensor alive
+        rp = L.route_params(K=s.K, logit_bias=bias_d)
+    else:
+        rp = L.route_params(mode=L.E0_ROUTE_SIGMOID_GROUP, K=s.K, n_groups=s.n_groups, topk_groups=s.topk_groups,
+                            scale=s.route_scale)
+    Y, inds, w, st = run_prefill(L, pool, dev(X), dev(W), rp, T)
+    assert st == 0
+    logits = O.router_logits(W, X, bias)
+    rt = O.route(logits, s)
+    ex, msgs = routing_matches(inds, w, rt)
+    assert not msgs, msgs[:4]
+    # tokens where both planted experts were selected, their order decided by
+    # a gap below 1e-4 and above the tie rule
+    both = [t for t in range(T) if t not in ex and e0 in rt.inds[t] and e1 in rt.inds[t]
+            and 0 < abs(logits[t, e0] - logits[t, e1]) < 1e-4]
+    assert len(both) >= (300 if mode == "softmax_topk" else 20), len(both)
+    sample = sorted(set(both[:12] + [0, T - 1]) - set(ex))
+    Yo, _ = O.prefill(X, bank, W, s, logit_bias=bias, tokens=sample)
+    assert max(rel_l2(Y[t], Yo[i]) for i, t in enumerate(sample)) <= REL_L2
+
+
 @pytest.fixture(scope="module")
 def prefill35(L):
     from int4_gathered_expert_gb300.model import SlotPoolDev
