@@ -46,6 +46,7 @@ struct PrefillWs {
     int32_t* seg_base;  // [nseg][E]
     int4* tiles;        // [max_tiles] {expert, first sorted row, n0, rows}, most rows first
     int32_t* flag;      // [T+1] tokens whose routing is recomputed in fp32 (count first)
+    int32_t* done;      // [T] row groups of a flagged token whose exact logits are written
     int32_t* n_tiles;   // [1]
     uint32_t* err;      // [1] timeouts inside the GEMMs
     float* wp;          // [T*K] routing weight per sorted row
@@ -79,6 +80,7 @@ static PrefillWs prefill_ws(char* base, int T, int H, int I, int E, int K) {
     w.seg_base = reinterpret_cast<int32_t*>(take(nseg * E * 4));
     w.tiles = reinterpret_cast<int4*>(take((size_t)w.max_tiles * 16));
     w.flag = reinterpret_cast<int32_t*>(take((size_t)(T + 1) * 4));
+    w.done = reinterpret_cast<int32_t*>(take((size_t)T * 4));
     w.n_tiles = reinterpret_cast<int32_t*>(take(16));
     w.err = reinterpret_cast<uint32_t*>(take(16));
     w.wp = reinterpret_cast<float*>(take(A * 4));
@@ -754,7 +756,7 @@ static size_t gemm2_smem() {
 // MAXM = ceil(E / 32) keys a lane.
 template <int MAXM>
 __global__ void __launch_bounds__(256) k_prefill_route(const float* logits, int T, int E, RouteP rp, int32_t* inds,
-                                                       float* w, int32_t* flag, uint32_t* st) {
+                                                       float* w, int32_t* flag, int32_t* done, uint32_t* st) {
     extern __shared__ float scr[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -763,29 +765,20 @@ __global__ void __launch_bounds__(256) k_prefill_route(const float* logits, int 
                                                w + (size_t)t * rp.K, scr + warp * E, st, lane);
     // a group count the ranking does not expect is always refined
     const bool odd = rp.mode == E0_ROUTE_SIGMOID_GROUP && (rp.n_groups < 1 || rp.n_groups > 32 || E % rp.n_groups);
-    if (lane == 0 && (odd || !(gap >= REFINE_GAP))) flag[1 + atomicAdd(flag, 1)] = t;
+    if (lane == 0 && (odd || !(gap >= REFINE_GAP))) {
+        const int i = atomicAdd(flag, 1);
+        flag[1 + i] = t;
+        done[i] = 0;
+    }
 }
 
 // fp16 row slice (64 halves) . fp16 x slice (64 halves), fp32 accumulation
-// Read-only 16-byte load kept in source order (volatile), so that all of a
-// lane's loads are issued before the first product: one memory round trip.
-E0_DEV uint4 ldg_nc_ordered(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
 E0_DEV float hh64_dot(const __half* wrow, const __half* x) {
-    uint4 wq[8], xq[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        wq[c] = ldg_nc_ordered(wrow + 8 * c);
-        xq[c] = ldg_nc_ordered(x + 8 * c);
-    }
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        const uint4 wv = wq[c];
-        const uint4 xv = xq[c];
+        const uint4 wv = ldg_stream(wrow + 8 * c);
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + 8 * c);
         const __half2* xh = reinterpret_cast<const __half2*>(&xv);
         float xs[8];
 #pragma unroll
@@ -799,52 +792,57 @@ E0_DEV float hh64_dot(const __half* wrow, const __half* x) {
     return acc;
 }
 
-// Exact (fp32 SIMT) logits of the flagged tokens: one warp per (token, row group).
-__global__ void __launch_bounds__(256) k_prefill_refine_logits(const __half* X, int H, const __half* W_r, int E,
-                                                               const int32_t* flag, float* logits) {
+// Exact (fp32 SIMT) logits of the flagged tokens, one warp per (token, row
+// group).  Each warp counts the row group it has written into done[i]; the
+// warp that completes token i's last one routes the token again from the
+// completed row (stores, fence, warp barrier, count: the fenced stores of
+// every lane come before the count another warp sees).  Four blocks an SM:
+// the grid is four blocks per SM.
+template <int MAXM>
+__global__ void __launch_bounds__(256, 4) k_prefill_refine(const __half* X, int H, const __half* W_r, int E, RouteP rp,
+                                                        const int32_t* flag, int32_t* done, float* logits,
+                                                        int32_t* inds, float* w, uint32_t* st) {
+    extern __shared__ float scr[];
     const int n = flag[0];
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const RowMap rm(H, lane);
     const int per_tok = (E + rm.R - 1) / rm.R;
     const long total = (long)n * per_tok;
-    for (long task = (long)blockIdx.x * 8 + (threadIdx.x >> 5); task < total; task += (long)gridDim.x * 8) {
-        const int t = flag[1 + task / per_tok];
+    for (long task = (long)blockIdx.x * 8 + warp; task < total; task += (long)gridDim.x * 8) {
+        const int i = (int)(task / per_tok);
+        const int t = flag[1 + i];
         const int e = (int)(task % per_tok) * rm.R + rm.r;
         float acc = 0.f;
         if (rm.active && e < E) acc = hh64_dot(W_r + (size_t)e * H + GROUP * rm.g, X + (size_t)t * H + GROUP * rm.g);
         acc = seg_sum(acc, rm.G, lane);
         if (rm.active && rm.g == 0 && e < E) logits[(size_t)t * E + e] = acc;
-    }
-}
-
-// Route the flagged tokens again from their exact logits (one warp each).
-template <int MAXM>
-__global__ void __launch_bounds__(256) k_prefill_reroute(const float* logits, int E, RouteP rp, const int32_t* flag,
-                                                         int32_t* inds, float* w, uint32_t* st) {
-    extern __shared__ float scr[];
-    const int n = flag[0];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int i = blockIdx.x * (blockDim.x >> 5) + warp; i < n; i += gridDim.x * (blockDim.x >> 5)) {
-        const int t = flag[1 + i];
-        route_warp_t<MAXM>(logits + (size_t)t * E, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K,
-                           scr + warp * E, st, lane);
+        __threadfence();
         __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&done[i], 1) == per_tok - 1;
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+            __threadfence();
+            route_warp_t<MAXM>(logits + (size_t)t * E, E, rp, inds + (size_t)t * rp.K, w + (size_t)t * rp.K,
+                               scr + warp * E, st, lane);
+            __syncwarp();
+        }
     }
 }
 
 // Both routing kernels, instantiated for the keys a lane holds (E / 32
 // rounded up to a power of two), so that no instance carries the registers
 // of a larger E.
-static void launch_route(bool again, const float* logits, int T, int E, const RouteP& rp, const int32_t* flag_in,
-                         int32_t* flag, int32_t* inds, float* w, uint32_t* st, cudaStream_t s) {
+static void launch_route(bool refine, const float* logits_in, float* logits, const __half* X, int H,
+                         const __half* W_r, int T, int E, const RouteP& rp, int32_t* flag, int32_t* done,
+                         int32_t* inds, float* w, uint32_t* st, cudaStream_t s) {
     const size_t sm = (size_t)8 * E * 4;
-    const unsigned grid = again ? (unsigned)num_sms() : (unsigned)((T + 7) / 8);
-#define E0_ROUTE_LAUNCH(M)                                                                    \
-    do {                                                                                      \
-        if (again)                                                                            \
-            k_prefill_reroute<M><<<grid, 256, sm, s>>>(logits, E, rp, flag_in, inds, w, st);  \
-        else                                                                                  \
-            k_prefill_route<M><<<grid, 256, sm, s>>>(logits, T, E, rp, inds, w, flag, st);    \
+#define E0_ROUTE_LAUNCH(M)                                                                                      \
+    do {                                                                                                        \
+        if (refine)                                                                                             \
+            k_prefill_refine<M><<<num_sms() * 4, 256, sm, s>>>(X, H, W_r, E, rp, flag, done, logits, inds, w,  \
+                                                               st);                                             \
+        else                                                                                                    \
+            k_prefill_route<M><<<(T + 7) / 8, 256, sm, s>>>(logits_in, T, E, rp, inds, w, flag, done, st);      \
     } while (0)
     if (E <= 32) E0_ROUTE_LAUNCH(1);
     else if (E <= 64) E0_ROUTE_LAUNCH(2);
@@ -1123,9 +1121,8 @@ int moe_prefill_forward(const uint16_t* Xu, int T, const e0_slot_pool* bank, con
     // 2. routing (+ refinement of near-ties)
     int32_t* flag = w.flag;
     if (cudaMemsetAsync(flag, 0, 4, s) != cudaSuccess) return E0_ERR_CUDA;
-    launch_route(false, w.logits, T, E, rp, nullptr, flag, inds, wts, st, s);
-    k_prefill_refine_logits<<<num_sms() * 4, 256, 0, s>>>(X, H, W_r, E, flag, w.logits);
-    launch_route(true, w.logits, T, E, rp, flag, nullptr, inds, wts, st, s);
+    launch_route(false, w.logits, w.logits, X, H, W_r, T, E, rp, flag, w.done, inds, wts, st, s);
+    launch_route(true, w.logits, w.logits, X, H, W_r, T, E, rp, flag, w.done, inds, wts, st, s);
     if (cudaGetLastError() != cudaSuccess) return E0_ERR_CUDA;
     // 3. sort
     int rc = sort_into(inds, T, K, E, w.counts, w.offsets, w.perm, w.pos, w, s);
