@@ -863,11 +863,13 @@ __global__ void k_prefill_tiles(const int32_t* counts, const int32_t* offsets, i
     // directions, so that the CTAs get similar loads.
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t part_rows[1024];
+    __shared__ int32_t part_rank[1024];
     const int e = threadIdx.x;
     const int c = e < E ? counts[e] : 0;
     const int nfull = c / BN, rem = c % BN;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     part_rows[e] = rem;
+    part_rank[e] = 0;
     // exclusive scan of the full tiles over the experts
     int incl = nfull;
 #pragma unroll
@@ -890,19 +892,25 @@ __global__ void k_prefill_tiles(const int32_t* counts, const int32_t* offsets, i
     const int start = incl - nfull + (warp > 0 ? warp_tot[warp - 1] : 0);
     const int n_full = warp_tot[(blockDim.x - 1) >> 5];
     for (int j = 0; j < nfull; ++j) tiles[start + j] = make_int4(e, offsets[e] + j * BN, j * BN, BN);
-    if (rem > 0) {
-        int rank = 0;
-        for (int f = 0; f < E; ++f) {
-            const int rf = part_rows[f];
-            rank += rf > rem || (rf == rem && f < e);
+    // rank of each partial tile: the partial tiles with more rows, and those
+    // with as many of a lower expert, come first.  Q = blockDim / E threads
+    // share an expert's count, each over E / Q of the others.
+    const int Q = max(1, (int)blockDim.x / E);
+    if ((int)threadIdx.x < Q * E) {
+        const int pe = threadIdx.x % E, q = threadIdx.x / E;
+        const int rem_e = part_rows[pe];
+        if (rem_e > 0) {
+            int r = 0;
+            for (int f = q * E / Q; f < (q + 1) * E / Q; ++f) {
+                const int rf = part_rows[f];
+                r += rf > rem_e || (rf == rem_e && f < pe);
+            }
+            if (r) atomicAdd(&part_rank[pe], r);
         }
-        tiles[n_full + rank] = make_int4(e, offsets[e] + nfull * BN, nfull * BN, rem);
     }
-    if (threadIdx.x == 0) {
-        int n_part = 0;
-        for (int f = 0; f < E; ++f) n_part += part_rows[f] > 0;
-        *n_tiles = n_full + n_part;
-    }
+    const int n_part = __syncthreads_count(rem > 0);
+    if (rem > 0) tiles[n_full + part_rank[e]] = make_int4(e, offsets[e] + nfull * BN, nfull * BN, rem);
+    if (threadIdx.x == 0) *n_tiles = n_full + n_part;
 }
 
 // xp[p] = X[token of perm[p]], wp[p] = w[perm[p]]
