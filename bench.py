@@ -619,10 +619,16 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_digest(kernel: str = "k_stack_ll"):
+    """Digest of a kernel's source files with comments and whitespace left
+    out: an edit that cannot change the compiled code keeps the digest."""
+    import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "int4_gathered_expert_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        h.update(open(os.path.join(d, f), "rb").read())
+        src = open(os.path.join(d, f), encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,8 +9,11 @@
 //   4. gather of the X rows into expert order;
 //   5. grouped GEMM gate/up on tcgen05 (int4 weights dequantised on chip into
 //      the 128-row M operand, tokens as the N operand), SwiGLU epilogue -> fp16;
-//   6. grouped GEMM down, epilogue scales by the routing weight -> fp32 rows;
-//   7. combine: Y[t] = sum over k (fixed order) of the token's K rows.
+//   6. grouped GEMM down, epilogue scales each row by its routing weight and
+//      adds it into Y[t] (fp32 atomics: the K terms of a token land in a
+//      varying order);
+//   7. with E0MOE_PREFILL_FIXED_ORDER=1 the rows go to an fp16 buffer
+//      instead and a combine sums a token's K rows in a fixed order.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdlib.h>
