@@ -111,14 +111,28 @@ __global__ void k_sort_hist(const int32_t* inds, int A, int E, int32_t* seg_cnt)
     for (int e = threadIdx.x; e < E; e += blockDim.x) seg_cnt[(size_t)blockIdx.x * E + e] = cnt[e];
 }
 
-// one block of 1024 threads: totals, exclusive scan over experts, per-segment bases
+// one block of 1024 threads: totals, exclusive scan over experts, per-segment
+// bases.  Q = blockDim / E threads share an expert: thread (q, e) walks the
+// segments [q nseg / Q, (q + 1) nseg / Q), so an expert's global loads run
+// Q at a time instead of one after another.
 __global__ void k_sort_scan(const int32_t* seg_cnt, int nseg, int E, int32_t* counts, int32_t* offsets,
                             int32_t* seg_base) {
     __shared__ int32_t warp_tot[32];
+    __shared__ int32_t part[1024];   // [q][e] count of expert e over thread (q, e)'s segments
+    __shared__ int32_t base_e[1024]; // exclusive scan of the totals
+    const int Q = max(1, (int)blockDim.x / E);
+    const int x = threadIdx.x, pe = x % E, q = x / E;
+    const bool walker = x < Q * E;
+    const int s0 = q * nseg / Q, s1 = (q + 1) * nseg / Q;
+    int pc = 0;
+    if (walker)
+        for (int s = s0; s < s1; ++s) pc += seg_cnt[(size_t)s * E + pe];
+    part[x] = pc;
+    __syncthreads();
     const int e = threadIdx.x;
     int c = 0;
     if (e < E)
-        for (int s = 0; s < nseg; ++s) c += seg_cnt[(size_t)s * E + e];
+        for (int j = 0; j < Q; ++j) c += part[j * E + e];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = c;
 #pragma unroll
@@ -142,13 +156,18 @@ __global__ void k_sort_scan(const int32_t* seg_cnt, int nseg, int E, int32_t* co
     if (e < E) {
         counts[e] = c;
         offsets[e] = excl;
-        int base = excl;
-        for (int s = 0; s < nseg; ++s) {
-            seg_base[(size_t)s * E + e] = base;
-            base += seg_cnt[(size_t)s * E + e];
-        }
+        base_e[e] = excl;
     }
     if (e == E - 1) offsets[E] = excl + c;
+    __syncthreads();
+    if (walker) {
+        int base = base_e[pe];
+        for (int j = 0; j < q; ++j) base += part[j * E + pe];
+        for (int s = s0; s < s1; ++s) {
+            seg_base[(size_t)s * E + pe] = base;
+            base += seg_cnt[(size_t)s * E + pe];
+        }
+    }
 }
 
 __global__ void k_sort_scatter(const int32_t* inds, int A, int E, const int32_t* seg_base, int32_t* perm,
