@@ -430,7 +430,10 @@ int e0_prefill_sort(const int32_t* inds, int T, int K, int E, int32_t* counts, i
                     int32_t* perm, void* ws, size_t ws_bytes, e0_stream_t stream);
 
 /* Prefill one layer for T tokens: route every token natively (logits =
- * W_router X + rp->logit_bias), sort assignments by expert, gather X rows,
+ * W_router X + rp->logit_bias, on the tensor cores with fp32 accumulation; a
+ * token whose K+1 largest scores, or whose G-th and (G+1)-th group scores,
+ * lie closer than 2e-4 is routed again from fp32 SIMT dot products, the
+ * precision of the decode path), sort assignments by expert, gather X rows,
  * run gate/up and down as grouped GEMMs on the tensor cores (fp16 operands,
  * weights dequantised on chip, fp32 accumulation), and form Y[t] =
  * sum_k w[t][k] expert(X[t]): added in fp32 with atomics (the order of the K
