@@ -342,40 +342,54 @@ def run_route_sweep(sd, X, n_warm: int = 8, n_timed: int = 96):
             "tokens": n_timed, "rows": rows}
 
 
-ORACLE_ONE_THREAD = r"""
-import gc, json, sys, time
-import numpy as np
-sys.path.insert(0, sys.argv[1])
-from oracle import e0_oracle as O
-from int4_gathered_expert_gb300 import synth
-res = {}
-def blk(d, T):
-    s = d["shape"]
-    hh = O.rmsnorm(d["x"][:T].astype(np.float64))
-    t0 = time.perf_counter()
-    rt = O.route_softmax_topk(O.router_logits(d["router"], hh), s.K)
-    O.moe_block(hh, O.BankExperts(d["bank"]), rt.inds, rt.w)
-    return time.perf_counter() - t0
-d = synth.tiny_layer(0, T=8)
-blk(d, 8)
-res["tiny_T8_ms"] = 1e3 * min(blk(d, 8) for _ in range(3))
-d = synth.layer35b(1, T=8)
-for T in (1, 8):
-    res["l35b_T%d_ms" % T] = 1e3 * blk(d, T)
-del d
-for name, shape in (("stack_8b", synth.STACK8B), ("stack_35b", synth.STACK35B)):
-    m = synth.stack_model(shape, n_tokens=2)
-    st = O.StackState(shape.n_layers)
-    t = []
-    for i in range(2):
+def oracle_config_timings(stacks):
+    """The oracle as it stands on the workloads other than the headline
+    line: one call of the routing + MoE block of the tiny layer (T=8, best
+    of three) and of the 35B-tier single layer (T=1, T=8), and, for each
+    named stack ("stack_8b", "stack_35b"), token 0 (every layer routes
+    natively) and one steady-state token; eight tokens are extrapolated as
+    token 0 + 7 steady tokens."""
+    import gc
+    from oracle import e0_oracle as O
+    from int4_gathered_expert_gb300 import synth
+    res = {}
+
+    def blk(d, T):
+        hh = O.rmsnorm(d["x"][:T].astype(np.float64))
         t0 = time.perf_counter()
-        O.stack_token(m.x[i], m, st)
-        t.append(time.perf_counter() - t0)
-    res[name] = {"token0_s": t[0], "steady_token_s": t[1], "tok_s": 1.0 / t[1],
-                 "tokens_8_s_extrapolated": t[0] + 7 * t[1]}
-    del m, st
-    gc.collect()
-print(json.dumps(res))
+        rt = O.route_softmax_topk(O.router_logits(d["router"], hh), d["shape"].K)
+        O.moe_block(hh, O.BankExperts(d["bank"]), rt.inds, rt.w)
+        return time.perf_counter() - t0
+
+    d = synth.tiny_layer(0, T=8)
+    blk(d, 8)
+    res["tiny_T8_ms"] = 1e3 * min(blk(d, 8) for _ in range(3))
+    d = synth.layer35b(1, T=8)
+    for T in (1, 8):
+        res["l35b_T%d_ms" % T] = 1e3 * blk(d, T)
+    del d
+    shapes = {"stack_8b": synth.STACK8B, "stack_35b": synth.STACK35B}
+    for name in stacks:
+        shape = shapes[name]
+        m = synth.stack_model(shape, n_tokens=2)
+        st = O.StackState(shape.n_layers)
+        t = []
+        for i in range(2):
+            t0 = time.perf_counter()
+            O.stack_token(m.x[i], m, st)
+            t.append(time.perf_counter() - t0)
+        res[name] = {"token0_s": t[0], "steady_token_s": t[1], "tok_s": 1.0 / t[1],
+                     "tokens_8_s_extrapolated": t[0] + 7 * t[1]}
+        del m, st
+        gc.collect()
+    return res
+
+
+ORACLE_ONE_THREAD = r"""
+import json, sys
+sys.path.insert(0, sys.argv[1])
+import bench
+print(json.dumps(bench.oracle_config_timings(("stack_8b", "stack_35b"))))
 """
 
 
@@ -843,13 +857,23 @@ def run_gb300(args):
         e2e = {"value": whole_job_rate(n_timed, ws, e2e_s), "unit": "tok/s", "h2d_bytes_per_step": tps * shape.layer.H * 4,
                "d2h_bytes_per_step": tps * shape.layer.H * 4}
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         n_cpu = 3
         el = time_oracle(model, n_cpu)
         cpu = {"value": n_cpu / el, "unit": "tok/s", "cores": cores(), "kind": "oracle",
                "sample": f"first {n_cpu} tokens of the same stream (token 0 routes all 40 layers natively) "
                          "through the 40-layer stack, float64 numpy oracle"}
+        try:
+            cpu_all = oracle_config_timings(("stack_8b",))
+            cpu_all.update({"cores": cores(), "kind": "oracle",
+                            "sample": "float64 numpy oracle on all host cores (numpy's BLAS threads): one call of "
+                                      "the routing + MoE block (tiny layer, 35B-tier layer); the 8B stack for "
+                                      "token 0 and one steady token, tokens_8_s_extrapolated = token 0 + 7 x "
+                                      "the steady token (extrapolated, not measured); the 35B stack is "
+                                      "cpu_baseline"})
+        except Exception as ex:  # a measurement that cannot run here is reported, not fatal
+            cpu_all = {"error": repr(ex)[:300]}
 
     sweep = None
     if rank == 0 and not args.no_extras and args.kernel_impl == 3 and args.layers == 40 and args.route_k == 4 \
@@ -913,7 +937,7 @@ def run_gb300(args):
                              "kernel": kname, "launch_us": mean_launch_s * 1e6,
                              "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback",
                              "peak_nominal": HBM_NOMINAL_GBS, "frac_nominal": achieved / HBM_NOMINAL_GBS},
-                "cpu_baseline": cpu, "cpu_oracle_one_thread": oracle1, "e2e": e2e, "prefill": prefill,
+                "cpu_baseline": cpu, "cpu_oracle_all_cores": cpu_all, "cpu_oracle_one_thread": oracle1, "e2e": e2e, "prefill": prefill,
                 "prefill_8b": prefill8, "stack_8b": stack8b, "block_35b": block, "route_sweep": sweep,
                 "streaming": streaming,
                 "gpu_launches": n_timed * LAUNCHES_PER_TOKEN.get(args.kernel_impl, 6 * shape.n_layers + 1),
